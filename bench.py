@@ -1,0 +1,379 @@
+#!/usr/bin/env python3
+"""Benchmark of the decode-attention hot path (fused qkv_post + decode attention,
+one fr_decode_attn call per step) on synthetic inputs of the documented
+workloads.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config pi05]
+                    [--impl ours|reference] [--no-cpu-baseline]
+
+Prints ONE JSON line (rank 0). `value` is device time per call in µs (lower is
+better), measured with CUDA events around K back-to-back calls replayed from a
+CUDA graph, with K/V, Q and mask rotated over replicas whose total exceeds
+2x L2, so every call streams its K/V from HBM. `e2e` is the same call made
+through the public API with pinned host buffers: host->device copies of that
+step's inputs and a device->host read of its output inside the timed region.
+
+`--impl reference` times the plain fp64 CPU oracle on the host cores on the
+same workload (each step = one oracle call), for the driver's ratio.
+"""
+import argparse
+import json
+import math
+import os
+import re
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+L2_BYTES = 129 * 1024 * 1024
+METRIC = "decode-attn µs/call (fused qkv_post + attention) and effective K/V HBM GB/s"
+
+
+def config_dict(w):
+    return {"workload": workload_desc(w), "name": w.name, "M": w.M, "hd": w.hd,
+            "n_kv": w.n_kv, "n_kv_real": w.n_kv_real}
+
+
+def workload_desc(w):
+    mask = {"none": "no mask", "causal": "causal mask", "random5": "random 5% -inf per token"}[w.mask_kind]
+    pad = f" padded to {w.n_kv}" if w.n_kv_real < w.n_kv else ""
+    yarn = (f", YaRN freq_scale={w.rope.freq_scale:g} ext_factor={w.rope.ext_factor:g} "
+            f"n_ctx_orig={w.rope.n_ctx_orig}") if w.rope.ext_factor else ""
+    return (f"{w.name}: n_head={w.n_head} sharing 1 KV head, hd={w.hd}, n_tok={w.n_tok}, "
+            f"n_kv={w.n_kv_real}{pad}, {mask}, NEOX RoPE base {w.rope.freq_base:g}{yarn}, "
+            f"positions {w.positions[0]}..{w.positions[-1]}")
+
+
+def algorithmic_bytes(w):
+    """Bytes one call must move at least: K+V (all n_kv rows the call is given),
+    Q f32 in, positions, mask, fp32 out."""
+    kv = 4 * w.n_kv * w.hd
+    q = 4 * w.M * w.hd
+    mask = 0 if w.mask() is None else 2 * w.n_tok * w.n_kv
+    out = 4 * w.M * w.hd
+    return kv + q + 4 * w.n_tok + mask + out, kv
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def kernel_source_hash():
+    import hashlib
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "gqa_kv_head_gb300", "csrc")
+    for fn in sorted(os.listdir(csrc)):
+        if fn.endswith((".cu", ".cuh")):
+            h.update(open(os.path.join(csrc, fn), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(config):
+    """DRAM bytes per launch from the committed ncu summary for this workload,
+    valid only while the kernel sources are unchanged since the capture."""
+    p = os.path.join(ROOT, "profiles", f"fr_decode_attn_{config}.md")
+    if not os.path.exists(p):
+        return None
+    txt = open(p).read()
+    m = re.search(r"traffic_bytes_per_launch:\s*(\d+)\s+source_sha:\s*([0-9a-f]+)", txt)
+    if not m or m.group(2) != kernel_source_hash():
+        return None
+    return int(m.group(1))
+
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax = float(parts[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        sm.sort()
+        med = sm[len(sm) // 2] if sm else None
+        return {"sm_mhz": med, "sm_max_mhz": smax, "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def cpu_oracle_time(config, budget_s, threads=1):
+    """Run the oracle on the full workload repeatedly for about budget_s seconds
+    in a child process with `threads` BLAS threads; returns (µs/call, calls)."""
+    env = dict(os.environ, OMP_NUM_THREADS=str(threads), OPENBLAS_NUM_THREADS=str(threads),
+               MKL_NUM_THREADS=str(threads))
+    code = (
+        "import sys, time, json; sys.path.insert(0, %r)\n"
+        "import gen, oracle\n"
+        "w = gen.make_workload(%r)\n"
+        "args = (w.q(), w.pos(), w.k(), w.v(), w.mask(), w.rope, w.q_scale, w.kq_scale)\n"
+        "oracle.decode_attn(*args)\n"
+        "n = 0; t0 = time.perf_counter()\n"
+        "while True:\n"
+        "    oracle.decode_attn(*args); n += 1\n"
+        "    if time.perf_counter() - t0 >= %f: break\n"
+        "print(json.dumps({'us': (time.perf_counter() - t0) / n * 1e6, 'calls': n}))\n"
+    ) % (ROOT, config, budget_s)
+    r = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True)
+    if r.returncode != 0:
+        raise RuntimeError("cpu oracle run failed: " + r.stderr[-2000:])
+    d = json.loads(r.stdout.strip().splitlines()[-1])
+    return d["us"], d["calls"]
+
+
+def run_reference(args, rank, world):
+    """The CPU oracle as the reference arm."""
+    import gen
+    import oracle
+    if rank != 0:
+        return
+    w = gen.make_workload(args.config)
+    inputs = (w.q(), w.pos(), w.k(), w.v(), w.mask(), w.rope, w.q_scale, w.kq_scale)
+    for _ in range(args.warmup):
+        oracle.decode_attn(*inputs)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.decode_attn(*inputs)
+    dt = time.perf_counter() - t0
+    us = dt / args.steps * 1e6
+    cores = int(os.environ.get("OPENBLAS_NUM_THREADS", "0")) or (os.cpu_count() or 1)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": us, "unit": "us/call",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": us / 1000.0, "higher_is_better": False, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": config_dict(w),
+        "cpu_baseline": {"value": us, "unit": "us/call", "cores": cores, "kind": "oracle",
+                         "sample": f"{args.steps} full oracle calls on the {w.name} workload"},
+        "e2e": {"value": us, "unit": "us/call", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args, rank, world, local_rank):
+    import numpy as np
+    import torch
+    import gen
+    import gqa_kv_head_gb300 as fr
+    from gqa_kv_head_gb300 import build as frbuild
+
+    frbuild.build()
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    w = gen.make_workload(args.config)
+    total_bytes, kv_bytes = algorithmic_bytes(w)
+    kv_real_bytes = 4 * w.n_kv_real * w.hd
+
+    # --- replicas over 2x L2 ------------------------------------------------
+    q_h = torch.from_numpy(w.q().reshape(w.n_tok, -1))
+    pos_h = torch.from_numpy(w.pos())
+    k_h = torch.from_numpy(w.k())
+    v_h = torch.from_numpy(w.v())
+    m_np = w.mask()
+    m_h = None if m_np is None else torch.from_numpy(m_np)
+    per_rep = total_bytes
+    n_rep = max(2, math.ceil(2 * L2_BYTES / per_rep))
+    reps = []
+    for _ in range(n_rep):
+        reps.append({
+            "q": q_h.to(dev), "pos": pos_h.to(dev), "k": k_h.to(dev), "v": v_h.to(dev),
+            "mask": None if m_h is None else m_h.to(dev)})
+    out = torch.empty((w.n_tok, w.n_head, w.hd), dtype=torch.float32, device=dev)
+    ws = fr.make_workspace(w.n_tok, w.n_head, w.hd, w.n_kv, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+
+    def call(r, st):
+        fr.decode_attn(r["k"], r["v"], w.n_tok, w.n_head, q=r["q"], pos=r["pos"], rope=w.rope,
+                       q_scale=w.q_scale, mask=r["mask"], kq_scale=w.kq_scale, out=out,
+                       workspace=ws, stream=st)
+
+    # eager warm-up (also checks the call works before capture)
+    with torch.cuda.stream(stream):
+        for i in range(max(3, args.warmup)):
+            call(reps[i % n_rep], stream)
+    stream.synchronize()
+
+    # --- graph of G calls rotating over the replicas --------------------------
+    G = min(args.steps, max(n_rep, 1000))
+    def capture(n):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for i in range(n):
+                call(reps[i % n_rep], stream)
+        return g
+    g_full = capture(G)
+    rem = args.steps % G
+    g_rem = capture(rem) if rem else None
+    n_full = args.steps // G
+    with torch.cuda.stream(stream):
+        g_full.replay()                       # graph warm-up
+    stream.synchronize()
+
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+    clocks = ClockSampler(local_rank)
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.15)
+    with torch.cuda.stream(stream):
+        ev0.record(stream)
+        for _ in range(n_full):
+            g_full.replay()
+        if g_rem is not None:
+            g_rem.replay()
+        ev1.record(stream)
+    stream.synchronize()
+    # keep the same replays running briefly so the sampler sees the load
+    t_end = time.perf_counter() + 0.6
+    with torch.cuda.stream(stream):
+        while time.perf_counter() < t_end:
+            g_full.replay()
+            stream.synchronize()
+    clk = clocks.stop()
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    ms = ev0.elapsed_time(ev1)
+    if dist:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    us_per_call = ms * 1000.0 / args.steps
+
+    # --- end to end through the public API with pinned host buffers ----------
+    q_p = q_h.pin_memory(); pos_p = pos_h.pin_memory(); k_p = k_h.pin_memory(); v_p = v_h.pin_memory()
+    m_p = None if m_h is None else m_h.pin_memory()
+    out_p = torch.empty(out.shape, dtype=torch.float32).pin_memory()
+    e2e_steps = min(args.steps, 200)
+    h2d = sum(t.numel() * t.element_size() for t in (q_p, pos_p, k_p, v_p) + ((m_p,) if m_p is not None else ()))
+    d2h = out_p.numel() * 4
+    def e2e_step(r):
+        r["q"].copy_(q_p, non_blocking=True); r["pos"].copy_(pos_p, non_blocking=True)
+        r["k"].copy_(k_p, non_blocking=True); r["v"].copy_(v_p, non_blocking=True)
+        if m_p is not None:
+            r["mask"].copy_(m_p, non_blocking=True)
+        call(r, stream)
+        out_p.copy_(out, non_blocking=True)
+    with torch.cuda.stream(stream):
+        for i in range(3):
+            e2e_step(reps[i % n_rep])
+        stream.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True); e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for i in range(e2e_steps):
+            e2e_step(reps[i % n_rep])
+        e1.record(stream)
+    stream.synchronize()
+    e2e_us = e0.elapsed_time(e1) * 1000.0 / e2e_steps
+
+    # --- CPU oracle baseline (rank 0 only, N = 1 only) -------------------------
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        us_cpu, n_cpu = cpu_oracle_time(args.config, args.cpu_seconds, threads=1)
+        cpu = {"value": us_cpu, "unit": "us/call", "cores": 1, "kind": "oracle",
+               "sample": f"{n_cpu} full oracle calls (fp64 numpy, 1 BLAS thread) on the "
+                         f"{w.name} workload, ~{args.cpu_seconds:.0f} s"}
+
+    peak, peak_kind = load_peaks()
+    achieved = total_bytes / (us_per_call * 1e-6) / 1e9
+    line = {
+        "metric": METRIC, "value": us_per_call, "unit": "us/call", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": us_per_call / 1000.0, "higher_is_better": False,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f16", "data": "synthetic",
+        "config": config_dict(w),
+        "timing": {"launch": f"CUDA graph of {G} back-to-back calls, replayed",
+                   "l2": f"inputs rotated over {n_rep} replicas ({n_rep * per_rep / 2**20:.0f} MiB > 2x L2)",
+                   "parallelism": "replicas only" if world > 1 else "1 GPU"},
+        "kv_gbs": kv_real_bytes / (us_per_call * 1e-6) / 1e9,
+        "kv_frac_of_hbm": kv_real_bytes / (us_per_call * 1e-6) / 1e9 / peak,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": ncu_traffic(args.config),
+                     "peak_kind": f"{peak_kind} hbm_gbs", "kernel": "fr::attn kernel (fused)",
+                     "algorithmic_bytes_per_launch": total_bytes},
+        "e2e": {"value": e2e_us, "unit": "us/call", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": args.steps,
+        "clocks": clk,
+    }
+    if cpu is not None:
+        line["cpu_baseline"] = cpu
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--config", default="pi05",
+                    help="tiny | pi05 | c3 | long_decode | sweep:hd:n_tok:n_kv")
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    try:
+        run_ours(args, rank, world, local_rank)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,118 @@
+// fr_common.cuh -- pieces shared by the qkv_post kernel and the decode
+// attention kernels: the RoPE table passed by value to every launch, the one
+// device routine that rotates a Q element pair (so the fused and the two-call
+// paths emit bit-identical f16 rows), argument checks and small PTX wrappers.
+#pragma once
+
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "fr_kernels.h"
+
+namespace fr {
+
+constexpr int kMaxPairs = 128;     // hd 256 -> 128 rotated pairs at most
+constexpr int kMaxTok = 16;        // q_tokens <= 16
+constexpr int kMaxRows = 512;      // M = n_tok * n_head
+
+// Per-launch RoPE constants (kernel parameter, by value).
+//   turns[i] = frac(w_i / 2pi) * 2^64, w_i = effective angle per position of
+//   pair i (base^(-2i/n_dims) times the YaRN interpolation factor). The angle
+//   of pair i at integer position p is then 2pi * ((p * turns[i]) mod 2^64) /
+//   2^64: the product wraps exactly modulo one turn, so large positions lose
+//   no precision to the range reduction.
+struct RopeTable {
+    uint64_t turns[kMaxPairs];
+    float mscale;       // attn_factor (* (1 + 0.1 ln(1/freq_scale)) with YaRN)
+    float q_scale;      // applied after the rotation
+    int half;           // n_dims / 2
+    int n_dims;
+};
+
+// Host: validate the parameters and fill the table. Returns false if invalid.
+bool build_rope_table(const fr_rope_params* rp, float q_scale, int hd, RopeTable* t);
+
+// Rotate (x0, x1) of pair i at position pos, then scale. Plain IEEE fp32 ops
+// with explicit rounding intrinsics so no contraction differs between the
+// kernels that call it.
+__device__ __forceinline__ void rope_pair(float x0, float x1, int pos, uint64_t turns,
+                                          float mscale, float q_scale,
+                                          float& y0, float& y1) {
+    const uint64_t a = (uint64_t)(int64_t)pos * turns;      // mod 2^64 = mod one turn
+    const float half_turns = (float)(int64_t)a * 0x1p-63f;   // angle / pi in [-1, 1)
+    float s, c;
+    sincospif(half_turns, &s, &c);
+    c = __fmul_rn(c, mscale);
+    s = __fmul_rn(s, mscale);
+    const float r0 = __fmaf_rn(x0, c, -__fmul_rn(x1, s));
+    const float r1 = __fmaf_rn(x0, s, __fmul_rn(x1, c));
+    y0 = __fmul_rn(r0, q_scale);
+    y1 = __fmul_rn(r1, q_scale);
+}
+
+// One "slot" of a Q row: slot c < half rotates dims (c, c + half); slot
+// c >= half passes dims n_dims + 2(c - half) and +1 through (scaled).
+// hd/2 slots cover the row exactly.
+__device__ __forceinline__ void rope_slot(const float* __restrict__ qrow, int c, int pos,
+                                          const RopeTable& tb, int& d0, int& d1,
+                                          float& y0, float& y1) {
+    if (c < tb.half) {
+        d0 = c;
+        d1 = c + tb.half;
+        rope_pair(qrow[d0], qrow[d1], pos, tb.turns[c], tb.mscale, tb.q_scale, y0, y1);
+    } else {
+        d0 = tb.n_dims + 2 * (c - tb.half);
+        d1 = d0 + 1;
+        y0 = __fmul_rn(qrow[d0], tb.q_scale);
+        y1 = __fmul_rn(qrow[d1], tb.q_scale);
+    }
+}
+
+inline bool aligned16(const void* p) { return (((uintptr_t)p) & 15u) == 0; }
+
+// ---- PTX wrappers ---------------------------------------------------------
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+// 16-byte async copy global -> shared; src_bytes 0 zero-fills the destination.
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, int src_bytes) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n"
+                 :: "r"(dst), "l"(src), "r"(src_bytes) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+    asm volatile("cp.async.commit_group;\n" ::: "memory");
+}
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;\n" :: "n"(N) : "memory");
+}
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1,
+                                        uint32_t& r2, uint32_t& r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3) : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1,
+                                          uint32_t& r2, uint32_t& r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3) : "r"(addr));
+}
+
+// D (16x8 f32) += A (16x16 f16, row) * B (16x8 f16, col)
+__device__ __forceinline__ void mma_16816(float* d, const uint32_t* a, uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
+        "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};\n"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
+    __half2 h = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&h);
+}
+
+}  // namespace fr

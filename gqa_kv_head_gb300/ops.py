@@ -1,0 +1,131 @@
+"""Python binding of the C ABI: argument marshalling only.
+
+Every function takes torch CUDA tensors, passes their device pointers, strides
+and the current CUDA stream to the library, and raises FrError on a non-OK
+status. All arithmetic happens in the library's kernels.
+"""
+import ctypes
+import math
+
+import torch
+
+from . import _abi
+from ._abi import FrError, FrRopeParams
+
+
+def rope_params(n_dims, freq_base=10000.0, freq_scale=1.0, ext_factor=0.0, attn_factor=1.0,
+                beta_fast=32.0, beta_slow=1.0, n_ctx_orig=4096):
+    return FrRopeParams(int(n_dims), float(freq_base), float(freq_scale), float(ext_factor),
+                        float(attn_factor), float(beta_fast), float(beta_slow), int(n_ctx_orig))
+
+
+def _as_rope(rp):
+    if rp is None or isinstance(rp, FrRopeParams):
+        return rp
+    return rope_params(rp.n_dims, rp.freq_base, rp.freq_scale, rp.ext_factor, rp.attn_factor,
+                       rp.beta_fast, rp.beta_slow, rp.n_ctx_orig)
+
+
+def _stream(stream):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _check_dev(*ts):
+    for t in ts:
+        if t is not None and not t.is_cuda:
+            raise ValueError("tensors must be CUDA tensors")
+
+
+def _q_tok_stride(q, n_head, hd):
+    """q is [n_tok, n_head, hd] (or [n_tok, >= n_head*hd]) f32 with unit inner strides."""
+    if q.dtype != torch.float32:
+        raise TypeError("q must be float32")
+    if q.dim() == 3:
+        if q.stride(2) != 1 or q.stride(1) != hd:
+            raise ValueError("q [n_tok, n_head, hd] needs contiguous heads")
+        return q.stride(0)
+    if q.dim() == 2 and q.stride(1) == 1:
+        return q.stride(0)
+    raise ValueError("q must be [n_tok, n_head, hd] or [n_tok, Nq]")
+
+
+def qkv_post(q, pos, n_head, hd, rope, q_scale=None, q16_out=None, q32_out=None, stream=None):
+    """fr_qkv_post. Returns (q16 [n_tok*n_head, hd] f16, q32 or None)."""
+    lib = _abi.load()
+    _check_dev(q, pos, q16_out, q32_out)
+    n_tok = q.shape[0]
+    if q_scale is None:
+        q_scale = 1.0 / math.sqrt(hd)
+    if q16_out is None:
+        q16_out = torch.empty((n_tok * n_head, hd), dtype=torch.float16, device=q.device)
+    rp = _as_rope(rope)
+    st = lib.fr_qkv_post(_ptr(q), _q_tok_stride(q, n_head, hd), _ptr(pos), n_tok, n_head, hd,
+                         ctypes.byref(rp), float(q_scale), _ptr(q16_out), _ptr(q32_out),
+                         _stream(stream))
+    _abi.check(st, "fr_qkv_post")
+    return q16_out, q32_out
+
+
+def workspace_size(n_tok, n_head, hd, n_kv):
+    return int(_abi.load().fr_decode_attn_workspace_size(n_tok, n_head, hd, n_kv))
+
+
+def make_workspace(n_tok, n_head, hd, n_kv, device="cuda", stream=None):
+    """Allocate (torch) and zero (library) a workspace for this shape."""
+    n = workspace_size(n_tok, n_head, hd, n_kv)
+    if n == 0:
+        raise FrError(2, "fr_decode_attn_workspace_size")
+    ws = torch.empty(n, dtype=torch.uint8, device=device)
+    _abi.check(_abi.load().fr_workspace_init(_ptr(ws), n, _stream(stream)), "fr_workspace_init")
+    return ws
+
+
+def workspace_check(ws, stream=None):
+    _abi.check(_abi.load().fr_workspace_check(_ptr(ws), _stream(stream)), "fr_workspace_check")
+
+
+def _row_stride(t, name):
+    if t.dim() != 2 or t.stride(1) != 1:
+        raise ValueError(f"{name} must be 2-D with unit inner stride")
+    return t.stride(0)
+
+
+def decode_attn(k, v, n_tok, n_head, *, q16=None, q=None, pos=None, rope=None, q_scale=None,
+                mask=None, kq_scale=1.0, out=None, workspace=None, splits=None, stream=None):
+    """fr_decode_attn (fused qkv_post when q16 is None). Returns out
+    [n_tok, n_head, hd] f32."""
+    lib = _abi.load()
+    _check_dev(k, v, q16, q, pos, mask, out, workspace)
+    n_kv, hd = k.shape[0], k.shape[1]
+    for name, t in (("k", k), ("v", v), ("mask", mask), ("q16", q16)):
+        if t is not None and t.dtype != torch.float16:
+            raise TypeError(f"{name} must be float16")
+    if out is None:
+        out = torch.empty((n_tok, n_head, hd), dtype=torch.float32, device=k.device)
+    if workspace is None:
+        workspace = make_workspace(n_tok, n_head, hd, n_kv, device=k.device, stream=stream)
+    q_stride = 0
+    rp = None
+    if q16 is None:
+        if q is None or pos is None or rope is None:
+            raise ValueError("pass q16, or q + pos + rope for the fused path")
+        q_stride = _q_tok_stride(q, n_head, hd)
+        rp = _as_rope(rope)
+        if q_scale is None:
+            q_scale = 1.0 / math.sqrt(hd)
+    args = [_ptr(q16), _ptr(q), q_stride, _ptr(pos), ctypes.byref(rp) if rp is not None else None,
+            float(q_scale or 0.0), _ptr(k), _row_stride(k, "k"), _ptr(v), _row_stride(v, "v"),
+            _ptr(mask), 0 if mask is None else _row_stride(mask, "mask"), n_tok, n_head, hd, n_kv,
+            float(kq_scale), _ptr(out), _ptr(workspace), workspace.numel()]
+    if splits is None:
+        st = lib.fr_decode_attn(*args, _stream(stream))
+        _abi.check(st, "fr_decode_attn")
+    else:
+        st = lib.fr_decode_attn_splits(*args, int(splits), _stream(stream))
+        _abi.check(st, "fr_decode_attn_splits")
+    return out

@@ -1,0 +1,184 @@
+/*
+ * fr_kernels.h -- C ABI of the GB300 (sm_103a) decode-attention hot path:
+ * qkv_post (NEOX RoPE with YaRN terms, 1/sqrt(hd) scale, f16 t-major Q rows)
+ * and the collapsed GQA decode attention over one shared f16 KV head.
+ *
+ * Plain C: raw pointers, sizes and a cudaStream_t; no framework types.
+ *
+ * Sources (the FlashRT pages):
+ *  - FlashRT PR #185 "ggml host adapter", commit "qkv_post optionally stores
+ *    the rope'd+scaled Q rows as f16": the [M, Nq] layout is the t-major order
+ *    the decode attention consumes; the f16 values round from the same fp32
+ *    registers.
+ *  - FlashRT PR #185, commit "FLASH_ATTN_EXT with q_tokens <= 16 over a single
+ *    padded f16 KV head": QK^T with a stride-0 K operand shared by the GQA
+ *    heads, a masked fp32-accurate softmax, PV whose fp32 result lands in the
+ *    node's [hd, n_head, n_tok] layout.
+ *  - FlashRT PR #185, commit "The GQA query heads share the one KV head": one
+ *    GEMM over all n_head*n_tok t-major rows; the PV output lands contiguously.
+ *  - FlashRT-llama.cpp development guide, "Architecture": launch interface with
+ *    raw pointers + cudaStream_t, consumable from plain C++; "Caches": no
+ *    allocation while a CUDA graph is being captured; "Invariants and
+ *    pitfalls": RoPE mirrors ggml's rope_neox with the YaRN corrections;
+ *    "SM120 target": runtime dimensions dispatched onto compile-time
+ *    specialisations at the launch boundary.
+ *
+ * Conventions for every entry point
+ *  - Device pointers unless stated otherwise; f16 tensors are IEEE binary16
+ *    stored as uint16_t. Every pointer and every row stride (in bytes) must be
+ *    16-byte aligned.
+ *  - Row index r = t*n_head + h ("t-major"): Q16 rows and output rows.
+ *  - Ownership: the caller owns every buffer. The library keeps no pointer
+ *    after a call returns, never allocates or frees device memory and holds no
+ *    mutable global state, so calls may be captured in a CUDA graph and made
+ *    from several host threads (each concurrent call needs its own workspace).
+ *  - Errors: arguments are validated on the host before any launch; an invalid
+ *    call returns a status != FR_OK and launches nothing. A failed launch
+ *    returns FR_ERR_CUDA. Nothing prints or aborts.
+ *  - Work is enqueued on `stream` and is asynchronous, like a kernel launch.
+ */
+#ifndef FR_KERNELS_H
+#define FR_KERNELS_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum fr_status {
+    FR_OK = 0,
+    FR_ERR_INVALID_ARG = 1,    /* null pointer, bad size, bad alignment or stride */
+    FR_ERR_UNSUPPORTED = 2,    /* valid but outside the supported shapes (hd, n_tok, M) */
+    FR_ERR_WORKSPACE = 3,      /* workspace missing or smaller than required */
+    FR_ERR_CUDA = 4,           /* a CUDA runtime call or a launch failed */
+    FR_ERR_DEVICE_TIMEOUT = 5  /* a bounded device-side wait gave up (see fr_workspace_check) */
+} fr_status;
+
+/* RoPE parameters, NEOX mode, with the YaRN terms as ggml's rope_ext takes
+ * them (FlashRT-llama.cpp development guide, "Invariants and pitfalls").
+ * Pair i < n_dims/2 rotates (x[i], x[i + n_dims/2]); dims >= n_dims pass
+ * through. theta_ext = pos * freq_base^(-2i/n_dims), theta_int = freq_scale *
+ * theta_ext; with ext_factor != 0 they are mixed by the YaRN ramp between the
+ * correction dims of beta_fast/beta_slow (n_ctx_orig) and the magnitude is
+ * attn_factor * (1 + 0.1 ln(1/freq_scale)); otherwise theta = theta_int and
+ * the magnitude is attn_factor. */
+typedef struct fr_rope_params {
+    int   n_dims;        /* rotated dims: even, 2 <= n_dims <= hd */
+    float freq_base;     /* > 0 */
+    float freq_scale;    /* > 0 */
+    float ext_factor;    /* YaRN mix strength; 0 = pure interpolation */
+    float attn_factor;
+    float beta_fast;
+    float beta_slow;
+    int   n_ctx_orig;    /* > 0 when ext_factor != 0 */
+} fr_rope_params;
+
+/* Human-readable name of a status code (static storage). */
+const char* fr_status_string(fr_status s);
+
+/* ABI version: (major << 16) | minor. */
+int fr_abi_version(void);
+
+/*
+ * fr_qkv_post -- the Q leg of qkv_post (FlashRT PR #185, commits "Fuses the
+ * prefix layers' q/k/v projections, RoPE, scale ..." and "qkv_post optionally
+ * stores the rope'd+scaled Q rows as f16").
+ *
+ *   q        f32, element (t, h, d) at q[t*q_tok_stride + h*hd + d]
+ *            (the QKV GEMM's [M = n_tok, Nq] rows; q_tok_stride >= n_head*hd,
+ *            a multiple of 4 elements)
+ *   pos      int32 [n_tok] token positions (shared by all heads of a token)
+ *   rp       RoPE parameters (host pointer, read during the call only)
+ *   q_scale  multiplier applied after the rotation (normally 1/sqrt(hd))
+ *   q16_out  f16 [n_tok*n_head][hd], row r = t*n_head + h, contiguous
+ *   q32_out  nullable; f32, same layout, the values q16_out is rounded from
+ *
+ * Arithmetic: angles reduced exactly modulo one turn (64-bit fixed point),
+ * rotation and scale in fp32, one round-to-nearest to f16.
+ * Supported: 1 <= n_tok <= 16, 1 <= n_head, M = n_tok*n_head <= 512,
+ * hd in {64, 128, 256}.
+ */
+fr_status fr_qkv_post(const float* q, int64_t q_tok_stride, const int32_t* pos,
+                      int n_tok, int n_head, int hd,
+                      const fr_rope_params* rp, float q_scale,
+                      uint16_t* q16_out, float* q32_out, cudaStream_t stream);
+
+/*
+ * Workspace bytes fr_decode_attn needs for this shape (0 for unsupported
+ * shapes). The workspace holds the split-KV partial states, self-resetting
+ * arrival tickets and a device status word. Zero it once after allocating it
+ * (fr_workspace_init); every call leaves the tickets at zero again.
+ */
+size_t fr_decode_attn_workspace_size(int n_tok, int n_head, int hd, int n_kv);
+
+/* Zero a freshly allocated workspace on `stream` (cudaMemsetAsync). */
+fr_status fr_workspace_init(void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/*
+ * Reads the workspace's device status word (synchronises `stream`), clears it
+ * and returns FR_ERR_DEVICE_TIMEOUT if a bounded device-side wait of an
+ * earlier call on this workspace gave up, else FR_OK.
+ */
+fr_status fr_workspace_check(void* workspace, cudaStream_t stream);
+
+/*
+ * fr_decode_attn -- decode attention for q_tokens <= 16 over one padded f16
+ * KV head shared by all n_head query heads (FlashRT PR #185, commits
+ * "FLASH_ATTN_EXT with q_tokens <= 16 ..." and "The GQA query heads share the
+ * one KV head ...").
+ *
+ * For every row r = t*n_head + h (M = n_tok*n_head rows):
+ *   s_j    = kq_scale * <Q16[r], K[j]> + mask[t][j]      j < n_kv
+ *   out[r] = sum_j softmax(s)_j V[j]                     fp32
+ * with fp32 accumulation and softmax. Columns whose mask is -inf get weight 0;
+ * a row whose every column is masked yields 0.
+ *
+ *   q16      f16 [M][hd], rope'd and scaled (fr_qkv_post's output), or NULL
+ *            to fuse qkv_post: then q, q_tok_stride, pos, rp and q_scale are
+ *            used exactly as in fr_qkv_post and the f16 rows are bit-identical
+ *            to what fr_qkv_post would have written.
+ *   k, v     f16 [n_kv][hd] with row strides k_row_stride / v_row_stride
+ *            (elements, >= hd, multiple of 8); one KV head, already rope'd.
+ *   mask     nullable; f16 additive [n_tok][n_kv], row stride mask_row_stride
+ *            (elements, >= n_kv, multiple of 8), shared by all heads
+ *            (ggml FA semantics with max_bias = 0 and softcap = 0).
+ *   out      f32 [n_tok][n_head][hd] contiguous == ggml [hd, n_head, n_tok].
+ *   workspace, workspace_bytes: >= fr_decode_attn_workspace_size(...), zeroed
+ *            once; one workspace per concurrently running call.
+ *
+ * Supported: 1 <= n_tok <= 16, M <= 512, hd in {64, 128, 256}, n_kv >= 1.
+ */
+fr_status fr_decode_attn(const uint16_t* q16,
+                         const float* q, int64_t q_tok_stride, const int32_t* pos,
+                         const fr_rope_params* rp, float q_scale,
+                         const uint16_t* k, int64_t k_row_stride,
+                         const uint16_t* v, int64_t v_row_stride,
+                         const uint16_t* mask, int64_t mask_row_stride,
+                         int n_tok, int n_head, int hd, int n_kv, float kq_scale,
+                         float* out, void* workspace, size_t workspace_bytes,
+                         cudaStream_t stream);
+
+/*
+ * Test and tuning hook (not needed by ordinary callers): fr_decode_attn with
+ * an explicit number of KV splits (0 = the library's choice; clamped to the
+ * number of KV tiles). Results agree with fr_decode_attn within fp32
+ * rounding-order differences.
+ */
+fr_status fr_decode_attn_splits(const uint16_t* q16,
+                                const float* q, int64_t q_tok_stride, const int32_t* pos,
+                                const fr_rope_params* rp, float q_scale,
+                                const uint16_t* k, int64_t k_row_stride,
+                                const uint16_t* v, int64_t v_row_stride,
+                                const uint16_t* mask, int64_t mask_row_stride,
+                                int n_tok, int n_head, int hd, int n_kv, float kq_scale,
+                                float* out, void* workspace, size_t workspace_bytes,
+                                int force_splits, cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FR_KERNELS_H */

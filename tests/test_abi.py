@@ -1,0 +1,130 @@
+"""The C-ABI library without a GPU: it builds, loads, exports every function
+include/fr_kernels.h declares, and rejects invalid arguments on the host
+before any CUDA call is made."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from gqa_kv_head_gb300 import build
+    build.build()
+    import gqa_kv_head_gb300 as fr
+    return fr.load()
+
+
+def _declared():
+    names = set()
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            src = open(os.path.join(ROOT, "include", fn)).read()
+            src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+            names |= set(re.findall(r"\b(fr_[a-z0-9_]+)\s*\(", src))
+    return names
+
+
+def test_exports_every_declared_symbol(lib):
+    names = _declared()
+    assert {"fr_qkv_post", "fr_decode_attn", "fr_decode_attn_workspace_size"} <= names
+    for n in sorted(names):
+        assert hasattr(lib, n), f"{n} declared in include/ but not exported"
+
+
+def test_library_is_in_tree(lib):
+    import gqa_kv_head_gb300 as fr
+    assert os.path.realpath(fr.library_path()).startswith(os.path.realpath(ROOT))
+
+
+def test_status_strings_and_version(lib):
+    assert lib.fr_status_string(0) == b"FR_OK"
+    for s in range(1, 6):
+        assert lib.fr_status_string(s).startswith(b"FR_ERR_")
+    assert lib.fr_abi_version() >> 16 == 1
+
+
+def test_workspace_size_host_logic(lib):
+    ws = lib.fr_decode_attn_workspace_size
+    assert ws(10, 8, 256, 1024) > 0
+    assert ws(17, 1, 128, 64) == 0          # q_tokens > 16
+    assert ws(16, 33, 128, 64) == 0         # M > 512
+    assert ws(1, 1, 96, 64) == 0            # unsupported hd
+    assert ws(1, 1, 128, 0) == 0
+    assert ws(16, 8, 128, 65536) >= ws(16, 8, 128, 4096) >= ws(16, 8, 128, 64)
+
+
+FAKE = 0x10000            # aligned, never dereferenced: validation fails first
+MIS = 0x10004
+
+
+def _rope(lib):
+    from gqa_kv_head_gb300 import rope_params
+    return rope_params(128)
+
+
+def _attn(lib, q16=FAKE, k=FAKE, v=FAKE, mask=None, k_rs=128, m_rs=0, n_tok=4, n_head=8,
+          hd=128, n_kv=64, ws=FAKE, ws_bytes=0, rp=None):
+    return lib.fr_decode_attn(q16, None, 0, None, rp, 0.0, k, k_rs, v, 128, mask, m_rs,
+                              n_tok, n_head, hd, n_kv, 1.0, FAKE, ws, ws_bytes, None)
+
+
+def test_decode_attn_validation(lib):
+    assert _attn(lib, k=None) == 1
+    assert _attn(lib, hd=96) == 2
+    assert _attn(lib, n_tok=17) == 2
+    assert _attn(lib, n_tok=16, n_head=33) == 2
+    assert _attn(lib, n_kv=0) == 1
+    assert _attn(lib, k_rs=100) == 1                 # stride not a multiple of 8
+    assert _attn(lib, k_rs=64) == 1                  # stride < hd
+    assert _attn(lib, k=MIS) == 1                    # misaligned pointer
+    assert _attn(lib, mask=FAKE, m_rs=32) == 1       # mask stride < n_kv
+    assert _attn(lib, ws=None) == 1
+    assert _attn(lib, ws_bytes=16) == 3              # workspace too small
+    # fused path without q/pos/rope
+    assert _attn(lib, q16=None) == 1
+    assert lib.fr_decode_attn_splits(FAKE, None, 0, None, None, 0.0, FAKE, 128, FAKE, 128, None,
+                                     0, 4, 8, 128, 64, 1.0, FAKE, FAKE, 0, -1, None) == 1
+
+
+def test_qkv_post_validation(lib):
+    rp = _rope(lib)
+    call = lambda **kw: lib.fr_qkv_post(kw.get("q", FAKE), kw.get("stride", 8 * 128),
+                                        kw.get("pos", FAKE), kw.get("n_tok", 4), 8,
+                                        kw.get("hd", 128), ctypes.byref(kw.get("rp", rp)),
+                                        0.1, kw.get("out", FAKE), None, None)
+    assert call(q=None) == 1
+    assert call(out=None) == 1
+    assert call(hd=80) == 2
+    assert call(n_tok=17) == 2
+    assert call(stride=8 * 128 - 4) == 1
+    assert call(stride=8 * 128 + 2) == 1
+    assert call(q=MIS) == 1
+    from gqa_kv_head_gb300 import rope_params
+    assert call(rp=rope_params(127)) == 1            # odd n_dims
+    assert call(rp=rope_params(256)) == 1            # n_dims > hd
+    assert call(rp=rope_params(128, freq_base=-1.0)) == 1
+    assert call(rp=rope_params(128, ext_factor=1.0, n_ctx_orig=0)) == 1
+
+
+def test_workspace_init_rejects_null(lib):
+    assert lib.fr_workspace_init(None, 4096, None) == 1
+    assert lib.fr_workspace_check(None, None) == 1
+
+
+def test_binding_has_no_cpu_path():
+    """The Python layer is marshalling only: no numpy/oracle import, and it
+    refuses CPU tensors instead of computing anything."""
+    import gqa_kv_head_gb300 as fr
+    pkg = os.path.dirname(fr.__file__)
+    for fn in os.listdir(pkg):
+        if fn.endswith(".py"):
+            src = open(os.path.join(pkg, fn)).read()
+            assert "import oracle" not in src and "from oracle" not in src, fn
+    import torch
+    with pytest.raises(ValueError):
+        fr.decode_attn(torch.zeros(4, 64, dtype=torch.float16), torch.zeros(4, 64, dtype=torch.float16),
+                       1, 1, q16=torch.zeros(1, 64, dtype=torch.float16))

@@ -1,0 +1,206 @@
+"""GPU parity of fr_decode_attn against the fp64 oracle, through the C ABI.
+
+Bar: max-abs <= 2e-3 and relative L2 <= 1e-3 for the fp32 output; bitwise
+equality where the pages claim it (fused qkv_post == the two-call form,
+masked/pad columns inert, head permutation) or where the arithmetic is exact
+(one key returns V[0])."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gen import RopeParams, SWEEP_HD, SWEEP_NKV, SWEEP_NTOK, Workload, make_workload, named_config
+import gqa_kv_head_gb300 as fr
+from fr_harness import assert_close, host_kv, oracle_out, run_fused, run_two_call, to_device
+
+pytestmark = pytest.mark.gpu
+
+
+def _out_rows(out):
+    return out.reshape(-1, out.shape[-1]).cpu().numpy().astype(np.float64)
+
+
+@pytest.mark.parametrize("name", ["tiny", "pi05", "c3", "long_decode"])
+def test_named_configs_full(name):
+    w = named_config(name)
+    d = to_device(w)
+    out = run_fused(w, d)
+    torch.cuda.synchronize()
+    assert_close(_out_rows(out), oracle_out(w), name)
+
+
+@pytest.mark.parametrize("name", ["tiny", "pi05", "c3", "long_decode"])
+def test_fused_equals_two_call_bitwise(name):
+    """FlashRT PR #185: the f16 Q from qkv_post is bit-identical to what the
+    attention's own gather would produce."""
+    w = named_config(name)
+    d = to_device(w)
+    a = run_fused(w, d)
+    b, _ = run_two_call(w, d)
+    torch.cuda.synchronize()
+    assert torch.equal(a, b)
+
+
+@pytest.mark.parametrize("hd", SWEEP_HD)
+@pytest.mark.parametrize("n_kv", SWEEP_NKV)
+def test_sweep_sampled_rows(hd, n_kv):
+    """Every sweep point at full size (seed 0); the oracle checks a sample of
+    rows, always including the first and last row of every token."""
+    for n_tok in SWEEP_NTOK:
+        w = make_workload(f"sweep:{hd}:{n_tok}:{n_kv}")
+        d = to_device(w)
+        out = _out_rows(run_fused(w, d))
+        rng = np.random.default_rng(n_tok * 7 + n_kv)
+        rows = np.unique(np.concatenate([
+            np.arange(w.n_tok) * w.n_head, np.arange(w.n_tok) * w.n_head + w.n_head - 1,
+            rng.integers(0, w.M, size=8)]))
+        assert_close(out[rows], oracle_out(w, rows=rows), w.name)
+
+
+@pytest.mark.parametrize("seed", range(20))
+def test_sweep_seeds_small(seed):
+    """20 seeds per sweep point at the sizes the oracle finishes quickly."""
+    for hd in SWEEP_HD:
+        for n_kv in (256, 1024):
+            for n_tok in (1, 16):
+                w = make_workload(f"sweep:{hd}:{n_tok}:{n_kv}", seed=seed)
+                out = _out_rows(run_fused(w, to_device(w)))
+                assert_close(out, oracle_out(w), f"{w.name} seed {seed}")
+
+
+@pytest.mark.parametrize("n_kv", [1, 7, 63, 65, 1000, 4097])
+@pytest.mark.parametrize("hd", [64, 128, 256])
+def test_ragged_kv_and_strides(n_kv, hd):
+    """Ragged KV lengths (partial last tile, partial mask chunk), padded K/V and
+    mask row strides, and Q rows read from a fused-QKV-shaped buffer."""
+    w = Workload(f"ragged{n_kv}", n_head=5, n_tok=7, hd=hd, n_kv=n_kv,
+                 rope=RopeParams(n_dims=hd, freq_base=10000.0),
+                 positions=tuple(range(n_kv - 1, n_kv + 6)), mask_kind="random5", seed=3)
+    d = to_device(w, k_pad=16, mask_pad=8, q_extra_heads=2)
+    out = _out_rows(run_fused(w, d))
+    assert_close(out, oracle_out(w), w.name)
+
+
+@pytest.mark.parametrize("hd", [64, 128, 256])
+@pytest.mark.parametrize("n_head,n_tok", [(1, 1), (32, 16), (3, 11)])
+def test_edge_shapes(hd, n_head, n_tok):
+    w = Workload("edge", n_head=n_head, n_tok=n_tok, hd=hd, n_kv=777,
+                 rope=RopeParams(n_dims=hd, freq_base=10000.0),
+                 positions=tuple(range(760, 760 + n_tok)), mask_kind="causal", seed=5)
+    out = _out_rows(run_fused(w, to_device(w)))
+    assert_close(out, oracle_out(w), f"edge {n_head}x{n_tok} hd{hd}")
+
+
+@pytest.mark.parametrize("name", ["pi05", "c3"])
+def test_split_invariance(name):
+    w = named_config(name)
+    d = to_device(w)
+    ref = oracle_out(w)
+    outs = []
+    for s in (1, 2, 3, 1000):
+        o = _out_rows(run_fused(w, d, splits=s))
+        assert_close(o, ref, f"{name} splits={s}")
+        outs.append(o)
+    for o in outs[1:]:
+        assert np.max(np.abs(o - outs[0])) < 1e-4      # fp32 summation order only
+
+
+def test_single_key_is_v0_bitwise():
+    w = Workload("one", n_head=4, n_tok=3, hd=128, n_kv=1, rope=RopeParams(n_dims=128),
+                 positions=(0, 5, 9), seed=2)
+    d = to_device(w)
+    out = run_fused(w, d)
+    torch.cuda.synchronize()
+    v0 = d["v"][0].float()
+    assert torch.equal(out.reshape(-1, 128), v0.expand(w.M, 128))
+
+
+def test_zero_q_is_mean_of_visible_v():
+    w = named_config("pi05")
+    d = to_device(w)
+    q16 = torch.zeros((w.M, w.hd), dtype=torch.float16, device="cuda")
+    out = _out_rows(fr.decode_attn(d["k"], d["v"], w.n_tok, w.n_head, q16=q16, mask=d["mask"]))
+    k, v = host_kv(w)
+    ref = oracle.attention_collapsed(np.zeros((w.M, w.hd)), k, v, w.mask(), w.n_tok, w.n_head)
+    assert_close(out, ref, "zero q")
+
+
+def test_masked_and_pad_columns_inert_bitwise():
+    """Pad rows zero and masked by -inf (FlashRT PR #185, qkv_post pads KV to
+    the KQ stride): replacing their contents with finite garbage changes nothing."""
+    w = named_config("pi05")
+    d = to_device(w)
+    a = run_fused(w, d)
+    d["k"][968:] = 37.0
+    d["v"][968:] = -1234.0
+    b = run_fused(w, d)
+    torch.cuda.synchronize()
+    assert torch.equal(a, b)
+
+
+def test_head_permutation_permutes_rows_bitwise():
+    """The collapsed GEMM treats every t-major row alike (FlashRT PR #185,
+    'numerically identical to the batched form')."""
+    w = named_config("c3")
+    d = to_device(w)
+    a = run_fused(w, d)
+    perm = torch.randperm(w.n_head, generator=torch.Generator().manual_seed(0))
+    q3 = d["q"].reshape(w.n_tok, w.n_head, w.hd)
+    d2 = dict(d, q=q3[:, perm.cuda(), :].contiguous().reshape(w.n_tok, -1))
+    b = run_fused(w, d2)
+    torch.cuda.synchronize()
+    assert torch.equal(a[:, perm.cuda(), :], b)
+
+
+def test_fully_masked_token_is_zero():
+    w = named_config("c3")
+    d = to_device(w)
+    d["mask"][3, :] = float("-inf")
+    out = run_fused(w, d)
+    torch.cuda.synchronize()
+    assert torch.all(torch.isfinite(out))
+    assert torch.equal(out[3], torch.zeros_like(out[3]))
+    others = [t for t in range(w.n_tok) if t != 3]
+    m = w.mask().copy()
+    m[3, :] = -np.inf
+    k, v = host_kv(w)
+    ref = oracle.decode_attn(w.q(), w.pos(), k, v, m, w.rope, w.q_scale).reshape(w.n_tok, w.n_head, -1)
+    assert_close(out.cpu().numpy()[others], ref[others], "other tokens")
+
+
+def test_repeated_calls_reuse_workspace():
+    """Arrival tickets reset themselves: back-to-back calls on one workspace
+    give identical results."""
+    w = named_config("c3")
+    d = to_device(w)
+    ws = fr.make_workspace(w.n_tok, w.n_head, w.hd, w.n_kv)
+    outs = [run_fused(w, d, workspace=ws).clone() for _ in range(3)]
+    torch.cuda.synchronize()
+    assert torch.equal(outs[0], outs[1]) and torch.equal(outs[1], outs[2])
+    fr.workspace_check(ws)
+
+
+def test_graph_capture_replay():
+    """No allocation inside the call: it can be captured and replayed."""
+    w = named_config("pi05")
+    d = to_device(w)
+    ws = fr.make_workspace(w.n_tok, w.n_head, w.hd, w.n_kv)
+    out = torch.empty((w.n_tok, w.n_head, w.hd), dtype=torch.float32, device="cuda")
+    ref = run_fused(w, d, workspace=ws).clone()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        run_fused(w, d, workspace=ws, out=out, stream=s)
+    out.zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(out, ref)
+
+
+def test_unsupported_returns_status():
+    w = named_config("tiny")
+    d = to_device(w)
+    with pytest.raises(fr.FrError):
+        fr.decode_attn(d["k"], d["v"], 17, 1, q16=torch.zeros((17, 64), dtype=torch.float16,
+                                                                device="cuda"))
