@@ -26,6 +26,11 @@ class FrRopeParams(ctypes.Structure):
                 ("beta_slow", ctypes.c_float), ("n_ctx_orig", ctypes.c_int)]
 
 
+class FrAttnOpts(ctypes.Structure):
+    _fields_ = [("engine", ctypes.c_int), ("force_splits", ctypes.c_int),
+                ("force_cluster", ctypes.c_int), ("wait_probe_iters", ctypes.c_int)]
+
+
 _P = ctypes.c_void_p
 _I = ctypes.c_int
 _I64 = ctypes.c_int64
@@ -44,7 +49,7 @@ SIGNATURES = {
     "fr_workspace_init": (_I, [_P, _SZ, _P]),
     "fr_workspace_check": (_I, [_P, _P]),
     "fr_decode_attn": (_I, _ATTN_ARGS + [_P]),
-    "fr_decode_attn_splits": (_I, _ATTN_ARGS + [_I, _P]),
+    "fr_decode_attn_ex": (_I, _ATTN_ARGS + [ctypes.POINTER(FrAttnOpts), _P]),
 }
 
 _lib = None

@@ -1,0 +1,51 @@
+// fr_attn.h -- internal interface between the fr_decode_attn entry point
+// (validation, planning, workspace layout) and the tensor-core kernel.
+#pragma once
+
+#include <cuda_fp16.h>
+#include <stdint.h>
+
+#include "fr_common.cuh"
+
+namespace fr {
+namespace tc {
+
+constexpr int kMaxClusters = 24;         // clusters per 128-row tile (workspace bound)
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // a wait gives up after ~2 s
+
+struct TcArgs {
+    const __half* q16;        // given f16 Q rows [M][hd], or null (fused RoPE from q)
+    const float* q;
+    int64_t q_tok_stride;
+    const int32_t* pos;
+    float* out;
+    float* part_o;            // [row_tiles][n_clusters][128][hd]
+    float2* part_ml;          // [row_tiles][n_clusters][128]
+    unsigned* tickets;        // [row_tiles][C]
+    unsigned* status;
+    int has_mask;
+    int n_tok, n_head, M, n_kv;
+    int n_tiles;              // KV tiles of tile_keys(hd) keys
+    int tiles_per_split;
+    int n_clusters;           // clusters per row tile
+    int C;                    // CTAs per cluster (splits per cluster)
+    float kq_log2;
+    uint64_t wait_limit_ns;
+    uint32_t probe_iters;
+};
+
+struct TcLaunch {
+    TcArgs args;
+    RopeTable tb;
+    const void* k;
+    const void* v;
+    const void* mask;
+    int64_t k_rs, v_rs, m_rs;
+    int row_tiles, splits;
+};
+
+int tile_keys(int hd);
+fr_status launch_tc(const TcLaunch& L, int hd, cudaStream_t stream);
+
+}  // namespace tc
+}  // namespace fr

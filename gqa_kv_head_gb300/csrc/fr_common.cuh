@@ -33,22 +33,33 @@ struct RopeTable {
 // Host: validate the parameters and fill the table. Returns false if invalid.
 bool build_rope_table(const fr_rope_params* rp, float q_scale, int hd, RopeTable* t);
 
-// Rotate (x0, x1) of pair i at position pos, then scale. Plain IEEE fp32 ops
-// with explicit rounding intrinsics so no contraction differs between the
-// kernels that call it.
-__device__ __forceinline__ void rope_pair(float x0, float x1, int pos, uint64_t turns,
-                                          float mscale, float q_scale,
-                                          float& y0, float& y1) {
+// Scaled cosine and sine of pair i at integer position pos.
+__device__ __forceinline__ void rope_cs(int pos, uint64_t turns, float mscale, float& c, float& s) {
     const uint64_t a = (uint64_t)(int64_t)pos * turns;      // mod 2^64 = mod one turn
     const float half_turns = (float)(int64_t)a * 0x1p-63f;   // angle / pi in [-1, 1)
-    float s, c;
     sincospif(half_turns, &s, &c);
     c = __fmul_rn(c, mscale);
     s = __fmul_rn(s, mscale);
-    const float r0 = __fmaf_rn(x0, c, -__fmul_rn(x1, s));
-    const float r1 = __fmaf_rn(x0, s, __fmul_rn(x1, c));
-    y0 = __fmul_rn(r0, q_scale);
-    y1 = __fmul_rn(r1, q_scale);
+}
+
+// The two rotated outputs of a pair, from the scaled cos/sin. Plain IEEE fp32
+// ops with explicit rounding intrinsics, so every kernel that calls these
+// produces the same bits.
+__device__ __forceinline__ float rope_lo(float x0, float x1, float c, float s, float q_scale) {
+    return __fmul_rn(__fmaf_rn(x0, c, -__fmul_rn(x1, s)), q_scale);
+}
+__device__ __forceinline__ float rope_hi(float x0, float x1, float c, float s, float q_scale) {
+    return __fmul_rn(__fmaf_rn(x0, s, __fmul_rn(x1, c)), q_scale);
+}
+
+// Rotate (x0, x1) of pair i at position pos, then scale.
+__device__ __forceinline__ void rope_pair(float x0, float x1, int pos, uint64_t turns,
+                                          float mscale, float q_scale,
+                                          float& y0, float& y1) {
+    float c, s;
+    rope_cs(pos, turns, mscale, c, s);
+    y0 = rope_lo(x0, x1, c, s, q_scale);
+    y1 = rope_hi(x0, x1, c, s, q_scale);
 }
 
 // One "slot" of a Q row: slot c < half rotates dims (c, c + half); slot

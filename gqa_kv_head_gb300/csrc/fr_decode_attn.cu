@@ -25,6 +25,7 @@
 #include <math.h>
 #include <string.h>
 
+#include "fr_attn.h"
 #include "fr_common.cuh"
 
 namespace fr {
@@ -375,10 +376,54 @@ static Plan make_plan(int M, int n_kv, int num_sms, int force_splits) {
     return p;
 }
 
-static size_t workspace_bytes_for(int M, int hd, int n_kv) {
+static size_t v1_workspace_bytes(int M, int hd, int n_kv) {
     const int n_tiles = (n_kv + kBN - 1) / kBN;
     const size_t splits = (size_t)min(n_tiles, kMaxSplits);
     return kWsHeader + splits * M * hd * sizeof(float) + splits * M * sizeof(float2);
+}
+
+static size_t tc_workspace_bytes(int M, int hd) {
+    const size_t row_tiles = (size_t)(M + 127) / 128;
+    const size_t slots = row_tiles * tc::kMaxClusters * 128;
+    return kWsHeader + slots * hd * sizeof(float) + slots * sizeof(float2);
+}
+
+static size_t workspace_bytes_for(int M, int hd, int n_kv) {
+    const size_t a = v1_workspace_bytes(M, hd, n_kv), b = tc_workspace_bytes(M, hd);
+    return a > b ? a : b;
+}
+
+// Splits and cluster size of the tensor-core kernel. One 128-row tile per
+// ceil(M/128); splits of a row tile form clusters of C CTAs; at most as many
+// CTAs as are co-resident for that cluster size (1 CTA per SM).
+struct TcPlan {
+    int row_tiles, n_tiles, C, n_clusters, splits, tiles_per_split;
+};
+
+static TcPlan make_tc_plan(int M, int hd, int n_kv, int num_sms, int force_splits, int force_cluster) {
+    TcPlan p;
+    const int bn = tc::tile_keys(hd);
+    p.row_tiles = (M + 127) / 128;
+    p.n_tiles = (n_kv + bn - 1) / bn;
+    int C = force_cluster > 0 ? force_cluster : 8;
+    while (C > 1 && C > p.n_tiles) C >>= 1;
+    int n_cl;
+    if (force_splits > 0) {
+        n_cl = (force_splits + C - 1) / C;
+    } else {
+        const int budget = C >= 8 ? (num_sms * 120) / 152 : (C == 4 ? (num_sms * 144) / 152 : num_sms);
+        n_cl = budget / (p.row_tiles * C);
+    }
+    n_cl = max(1, min(n_cl, min(tc::kMaxClusters, (p.n_tiles + C - 1) / C)));
+    int S = C * n_cl;
+    p.tiles_per_split = (p.n_tiles + S - 1) / S;
+    // drop clusters that would get no tile at all
+    const int used = (p.n_tiles + p.tiles_per_split - 1) / p.tiles_per_split;
+    n_cl = max(1, (used + C - 1) / C);
+    p.C = C;
+    p.n_clusters = n_cl;
+    p.splits = C * n_cl;
+    return p;
 }
 
 template <int HD>
@@ -406,7 +451,13 @@ static fr_status decode_attn_impl(const uint16_t* q16, const float* q, int64_t q
                                   const uint16_t* k, int64_t k_rs, const uint16_t* v, int64_t v_rs,
                                   const uint16_t* mask, int64_t m_rs, int n_tok, int n_head, int hd,
                                   int n_kv, float kq_scale, float* out, void* ws, size_t ws_bytes,
-                                  int force_splits, cudaStream_t stream) {
+                                  const fr_attn_opts* opts, cudaStream_t stream) {
+    fr_attn_opts o = {0, 0, 0, 0};
+    if (opts) o = *opts;
+    if (o.engine < 0 || o.engine > 1 || o.force_splits < 0 || o.wait_probe_iters < 0) return FR_ERR_INVALID_ARG;
+    if (o.force_cluster != 0 && o.force_cluster != 1 && o.force_cluster != 2 && o.force_cluster != 4 &&
+        o.force_cluster != 8)
+        return FR_ERR_INVALID_ARG;
     if (!k || !v || !out || !ws) return FR_ERR_INVALID_ARG;
     if (n_tok < 1 || n_head < 1 || n_kv < 1) return FR_ERR_INVALID_ARG;
     if (hd != 64 && hd != 128 && hd != 256) return FR_ERR_UNSUPPORTED;
@@ -432,9 +483,48 @@ static fr_status decode_attn_impl(const uint16_t* q16, const float* q, int64_t q
     int dev = 0, sms = 152;
     if (cudaGetDevice(&dev) != cudaSuccess) return FR_ERR_CUDA;
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return FR_ERR_CUDA;
-    const Plan p = make_plan(M, n_kv, sms, force_splits);
-
     unsigned char* w = static_cast<unsigned char*>(ws);
+
+    if (o.engine == 0) {
+        const TcPlan p = make_tc_plan(M, hd, n_kv, sms, o.force_splits, o.force_cluster);
+        const size_t slots = (size_t)p.row_tiles * p.n_clusters * 128;
+        tc::TcLaunch L;
+        memset(&L, 0, sizeof(L));
+        tc::TcArgs& a = L.args;
+        a.q16 = reinterpret_cast<const __half*>(q16);
+        a.q = q;
+        a.q_tok_stride = q_tok_stride;
+        a.pos = pos;
+        a.out = out;
+        a.status = reinterpret_cast<unsigned*>(w);
+        a.tickets = reinterpret_cast<unsigned*>(w + kWsTickets);
+        a.part_o = reinterpret_cast<float*>(w + kWsHeader);
+        a.part_ml = reinterpret_cast<float2*>(w + kWsHeader + slots * hd * sizeof(float));
+        a.has_mask = mask != nullptr;
+        a.n_tok = n_tok;
+        a.n_head = n_head;
+        a.M = M;
+        a.n_kv = n_kv;
+        a.n_tiles = p.n_tiles;
+        a.tiles_per_split = p.tiles_per_split;
+        a.n_clusters = p.n_clusters;
+        a.C = p.C;
+        a.kq_log2 = kq_scale * kLog2e;
+        a.wait_limit_ns = tc::kWaitLimitNs;
+        a.probe_iters = (uint32_t)o.wait_probe_iters;
+        L.tb = tb;
+        L.k = k;
+        L.v = v;
+        L.mask = mask;
+        L.k_rs = k_rs;
+        L.v_rs = v_rs;
+        L.m_rs = m_rs;
+        L.row_tiles = p.row_tiles;
+        L.splits = p.splits;
+        return tc::launch_tc(L, hd, stream);
+    }
+
+    const Plan p = make_plan(M, n_kv, sms, o.force_splits);
     const size_t splits_cap = (size_t)min(p.n_tiles, kMaxSplits);
     AttnArgs a;
     a.q16 = reinterpret_cast<const __half*>(q16);
@@ -501,19 +591,17 @@ extern "C" fr_status fr_decode_attn(const uint16_t* q16, const float* q, int64_t
                                     size_t workspace_bytes, cudaStream_t stream) {
     return decode_attn_impl(q16, q, q_tok_stride, pos, rp, q_scale, k, k_row_stride, v, v_row_stride,
                             mask, mask_row_stride, n_tok, n_head, hd, n_kv, kq_scale, out, workspace,
-                            workspace_bytes, 0, stream);
+                            workspace_bytes, nullptr, stream);
 }
 
-extern "C" fr_status fr_decode_attn_splits(const uint16_t* q16, const float* q, int64_t q_tok_stride,
-                                           const int32_t* pos, const fr_rope_params* rp, float q_scale,
-                                           const uint16_t* k, int64_t k_row_stride, const uint16_t* v,
-                                           int64_t v_row_stride, const uint16_t* mask,
-                                           int64_t mask_row_stride, int n_tok, int n_head, int hd,
-                                           int n_kv, float kq_scale, float* out, void* workspace,
-                                           size_t workspace_bytes, int force_splits,
-                                           cudaStream_t stream) {
-    if (force_splits < 0) return FR_ERR_INVALID_ARG;
+extern "C" fr_status fr_decode_attn_ex(const uint16_t* q16, const float* q, int64_t q_tok_stride,
+                                       const int32_t* pos, const fr_rope_params* rp, float q_scale,
+                                       const uint16_t* k, int64_t k_row_stride, const uint16_t* v,
+                                       int64_t v_row_stride, const uint16_t* mask, int64_t mask_row_stride,
+                                       int n_tok, int n_head, int hd, int n_kv, float kq_scale, float* out,
+                                       void* workspace, size_t workspace_bytes, const fr_attn_opts* opts,
+                                       cudaStream_t stream) {
     return decode_attn_impl(q16, q, q_tok_stride, pos, rp, q_scale, k, k_row_stride, v, v_row_stride,
                             mask, mask_row_stride, n_tok, n_head, hd, n_kv, kq_scale, out, workspace,
-                            workspace_bytes, force_splits, stream);
+                            workspace_bytes, opts, stream);
 }

@@ -163,19 +163,27 @@ fr_status fr_decode_attn(const uint16_t* q16,
 
 /*
  * Test and tuning hook (not needed by ordinary callers): fr_decode_attn with
- * an explicit number of KV splits (0 = the library's choice; clamped to the
- * number of KV tiles). Results agree with fr_decode_attn within fp32
- * rounding-order differences.
+ * explicit choices. Results agree with fr_decode_attn within fp32
+ * rounding-order differences. opts may be NULL (all defaults).
  */
-fr_status fr_decode_attn_splits(const uint16_t* q16,
-                                const float* q, int64_t q_tok_stride, const int32_t* pos,
-                                const fr_rope_params* rp, float q_scale,
-                                const uint16_t* k, int64_t k_row_stride,
-                                const uint16_t* v, int64_t v_row_stride,
-                                const uint16_t* mask, int64_t mask_row_stride,
-                                int n_tok, int n_head, int hd, int n_kv, float kq_scale,
-                                float* out, void* workspace, size_t workspace_bytes,
-                                int force_splits, cudaStream_t stream);
+typedef struct fr_attn_opts {
+    int engine;            /* 0 = default (tcgen05 tensor-core kernel); 1 = mma.sync kernel */
+    int force_splits;      /* 0 = library's choice; else KV splits per 128-row tile */
+    int force_cluster;     /* 0 = library's choice; else 1, 2, 4 or 8 CTAs per cluster */
+    int wait_probe_iters;  /* > 0: every CTA also polls, this many times, a barrier that is
+                              never signalled; fr_workspace_check then reports
+                              FR_ERR_DEVICE_TIMEOUT (exercises the timeout path) */
+} fr_attn_opts;
+
+fr_status fr_decode_attn_ex(const uint16_t* q16,
+                            const float* q, int64_t q_tok_stride, const int32_t* pos,
+                            const fr_rope_params* rp, float q_scale,
+                            const uint16_t* k, int64_t k_row_stride,
+                            const uint16_t* v, int64_t v_row_stride,
+                            const uint16_t* mask, int64_t mask_row_stride,
+                            int n_tok, int n_head, int hd, int n_kv, float kq_scale,
+                            float* out, void* workspace, size_t workspace_bytes,
+                            const fr_attn_opts* opts, cudaStream_t stream);
 
 #ifdef __cplusplus
 }
