@@ -50,6 +50,7 @@ SIGNATURES = {
     "fr_workspace_check": (_I, [_P, _P]),
     "fr_decode_attn": (_I, _ATTN_ARGS + [_P]),
     "fr_decode_attn_ex": (_I, _ATTN_ARGS + [ctypes.POINTER(FrAttnOpts), _P]),
+    "fr_decode_attn_noalloc": (_I, _ATTN_ARGS[:18] + [_P]),
 }
 
 _lib = None

@@ -132,3 +132,32 @@ def decode_attn(k, v, n_tok, n_head, *, q16=None, q=None, pos=None, rope=None, q
         st = lib.fr_decode_attn_ex(*args, ctypes.byref(opts), _stream(stream))
         _abi.check(st, "fr_decode_attn_ex")
     return out
+
+
+def decode_attn_noalloc(k, v, n_tok, n_head, *, q16=None, q=None, pos=None, rope=None, q_scale=None,
+                        mask=None, kq_scale=1.0, out=None, stream=None):
+    """fr_decode_attn_noalloc: the same attention without a workspace, for
+    callers that cannot allocate device memory (the library's fixed scratch is
+    used instead; see include/fr_kernels.h for its limit and sharing rules).
+    Returns out [n_tok, n_head, hd] f32 (allocated here only if not given)."""
+    lib = _abi.load()
+    _check_dev(k, v, q16, q, pos, mask, out)
+    n_kv, hd = k.shape[0], k.shape[1]
+    if out is None:
+        out = torch.empty((n_tok, n_head, hd), dtype=torch.float32, device=k.device)
+    q_stride = 0
+    rp = None
+    if q16 is None:
+        if q is None or pos is None or rope is None:
+            raise ValueError("pass q16, or q + pos + rope for the fused path")
+        q_stride = _q_tok_stride(q, n_head, hd)
+        rp = _as_rope(rope)
+        if q_scale is None:
+            q_scale = 1.0 / math.sqrt(hd)
+    st = lib.fr_decode_attn_noalloc(
+        _ptr(q16), _ptr(q), q_stride, _ptr(pos), ctypes.byref(rp) if rp is not None else None,
+        float(q_scale or 0.0), _ptr(k), _row_stride(k, "k"), _ptr(v), _row_stride(v, "v"), _ptr(mask),
+        0 if mask is None else _row_stride(mask, "mask"), n_tok, n_head, hd, n_kv, float(kq_scale),
+        _ptr(out), _stream(stream))
+    _abi.check(st, "fr_decode_attn_noalloc")
+    return out

@@ -185,6 +185,32 @@ fr_status fr_decode_attn_ex(const uint16_t* q16,
                             float* out, void* workspace, size_t workspace_bytes,
                             const fr_attn_opts* opts, cudaStream_t stream);
 
+/*
+ * fr_decode_attn_noalloc -- fr_decode_attn without a workspace argument, for
+ * callers that cannot allocate device memory (their memory is planned up front
+ * by an allocator they do not control, or they must not allocate once running).
+ * The FlashRT pages have no counterpart to this entry point.
+ *
+ * Same arguments and result as fr_decode_attn, minus the workspace. The split
+ * state lives in a 9 MiB scratch array inside the library, present on every GPU
+ * that loads the library until the process exits. Shapes whose
+ * fr_decode_attn_workspace_size() exceeds 9 MiB (in practice hd = 256 with
+ * n_tok*n_head > 256) return FR_ERR_WORKSPACE. No device memory is allocated.
+ * The first call on each device looks up the array's device address
+ * (cudaGetSymbolAddress); make that first call before any stream capture. Each
+ * call clears the array's status word and arrival tickets on `stream` before
+ * launching. Every call shares the one array: calls that overlap on the GPU
+ * (other streams, other host threads) race and must be serialised by the caller.
+ */
+fr_status fr_decode_attn_noalloc(const uint16_t* q16,
+                                 const float* q, int64_t q_tok_stride, const int32_t* pos,
+                                 const fr_rope_params* rp, float q_scale,
+                                 const uint16_t* k, int64_t k_row_stride,
+                                 const uint16_t* v, int64_t v_row_stride,
+                                 const uint16_t* mask, int64_t mask_row_stride,
+                                 int n_tok, int n_head, int hd, int n_kv, float kq_scale,
+                                 float* out, cudaStream_t stream);
+
 #ifdef __cplusplus
 }
 #endif
