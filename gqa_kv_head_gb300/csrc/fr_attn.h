@@ -14,10 +14,7 @@ constexpr int kMaxClusters = 24;         // clusters per 128-row tile (workspace
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // a wait gives up after ~2 s
 
 struct TcArgs {
-    const __half* q16;        // given f16 Q rows [M][hd], or null (fused RoPE from q)
-    const float* q;
-    int64_t q_tok_stride;
-    const int32_t* pos;
+    const __half* q16;        // f16 Q rows [M][hd] (given, or qkv_post's output)
     float* out;
     float* part_o;            // [row_tiles][n_clusters][128][hd]
     float2* part_ml;          // [row_tiles][n_clusters][128]
@@ -36,7 +33,7 @@ struct TcArgs {
 
 struct TcLaunch {
     TcArgs args;
-    RopeTable tb;
+    bool pdl;                 // launched right after the qkv_post grid that writes q16
     const void* k;
     const void* v;
     const void* mask;

@@ -9,23 +9,29 @@
 // collapse into single GEMMs over all n_head*n_tok query rows".
 //
 // One CTA = 128 query rows (the MMA M; rows >= M are zero) x one KV split.
-// Warp roles (192 threads):
-//   warps 0-3  softmax: thread i owns TMEM lane i = query row i. Reads its S
-//              row, applies kq_scale and the mask, keeps the running max m and
-//              sum l (lazy rescale of O only when the max grows by > 2^8), and
-//              writes P back into TMEM as two f16 terms, P = P_hi + P_lo
-//              (P_lo = f16(p - P_hi)), so the weights keep ~22 bits and the
-//              softmax stays fp32-accurate even where |V| is large.
-//   warp 4     TMA producer: K, V and mask tiles into a ring of stages.
-//   warp 5     MMA issuer: S_j = Q K_j^T (SS form, S double-buffered in TMEM),
+// Warp roles (320 threads):
+//   warps 0-7  softmax: TMEM lane i = query row i is shared by warps i/32 and
+//              i/32 + 4, each taking half of the S tile's columns; the halves
+//              exchange their maxima per tile. Applies kq_scale and the mask,
+//              keeps the running max m and sum l (lazy rescale of O only when
+//              the max grows by > 2^8), and writes P back into TMEM as two f16
+//              terms, P = P_hi + P_lo (P_lo = f16(p - P_hi)), so the weights
+//              keep ~22 bits and the softmax stays fp32-accurate even where |V|
+//              is large.
+//   warp 8     TMA producer: K, V and mask tiles into a ring of stages; the
+//              first tiles are requested before the Q prologue.
+//   warp 9     MMA issuer: S_j = Q K_j^T (SS form, S double-buffered in TMEM),
 //              O += P_hi,j V_j + P_lo,j V_j (A operand from TMEM, V read
 //              MN-major), commits.
 // Splits of one row tile form thread-block clusters of C CTAs (cluster dim y):
-//   prologue   each CTA ropes 1/C of the Q rows (fused qkv_post) and stores
-//              the f16 rows into every peer's shared memory (DSMEM); with given
-//              f16 Q rows each CTA multicasts its 1/C slice by TMA instead.
-//   epilogue   the C partial states (m, l, O) are merged over DSMEM; CTA rank c
-//              owns rows [c*128/C, (c+1)*128/C). With several clusters per row
+//   prologue   each CTA multicasts its 1/C slice of the f16 Q rows by TMA. In
+//              the fused call the rows come from the qkv_post kernel launched
+//              just before (programmatic dependent launch: this kernel's set-up
+//              and first K/V loads overlap it).
+//   epilogue   each CTA stores its (m, l, O) rows straight from TMEM into the
+//              shared memory of the CTA that owns them (rank c owns rows
+//              [c*128/C, (c+1)*128/C)); owners merge the C states locally, in
+//              rank order. With several clusters per row
 //              tile the merged slices go to the workspace and the last CTA to
 //              arrive for each (row tile, rank) slice merges them (atomic ticket,
 //              reset afterwards). No CTA ever waits for another cluster.
@@ -47,9 +53,11 @@ namespace tc {
 using namespace sm100;
 
 constexpr int kRows = 128;
-constexpr int kThreads = 192;
-constexpr int kProdWarp = 4;
-constexpr int kMmaWarp = 5;
+constexpr int kSmaxWarps = 8;                // two warps per TMEM lane quadrant
+constexpr int kSmaxThreads = kSmaxWarps * 32;
+constexpr int kProdWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr int kThreads = (kSmaxWarps + 2) * 32;
 constexpr float kTau = 8.0f;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr uint32_t kTmemCols = 512;
@@ -67,10 +75,21 @@ struct Cfg {
     static constexpr int MASK_BYTES = (BN / 64) * MASK_BOX;
     static constexpr int STAGE_BYTES = 2 * K_BYTES + MASK_BYTES;
     static constexpr int BODY = Q_BYTES + STAGES * STAGE_BYTES;
-    static constexpr int RED_STRIDE = HD + 4;              // fp32 staging row stride
-    static constexpr int RED_BYTES = kRows * RED_STRIDE * 4 + kRows * 8;
-    static constexpr int DATA = BODY > RED_BYTES ? BODY : RED_BYTES;
-    static constexpr int AUX = 16384;                      // cos/sin table, then merge weights
+    static constexpr int DATA = BODY;
+    static constexpr int AUX = 20480;                      // cos/sin table; then exchange + merge weights
+    static constexpr int AUX_MAXX = 0;                     // [2][2][128] f32 half-row maxima
+    static constexpr int AUX_LX = 2048;                    // [2][128] f32 half-row sums
+    static constexpr int AUX_ML = 3072;                    // [C][R] (m, l) pushed by the cluster's CTAs
+    static constexpr int AUX_W = 4096;                     // merge weights (<= 16 KiB)
+    // After the KV loop, each CTA stores its O rows straight into the shared
+    // memory of the CTA that owns them: [C][R][RS] fp32 at RECV_OFF (past the
+    // Q tile). Each softmax warp transposes its rows through a 32 x 36 fp32
+    // buffer at TB_OFF so that its DSMEM stores write whole 128-byte segments.
+    static constexpr int RS = HD + 4;
+    static constexpr int RECV_OFF = Q_BYTES;
+    static constexpr int RECV_BYTES = kRows * RS * 4;
+    static constexpr int TB_BYTES = 8 * 32 * 36 * 4;
+    static constexpr int TB_OFF = HD == 256 ? 0 : RECV_OFF + RECV_BYTES;
     static constexpr int BAR_OFF = DATA + AUX;
     // mbarrier slots (8 bytes each), laid out from STAGES
     static constexpr int B_FULL = 0, B_EMPTY = STAGES, B_SFULL = 2 * STAGES, B_PFULL = 2 * STAGES + 2,
@@ -78,6 +97,8 @@ struct Cfg {
                          B_MMADONE = 2 * STAGES + 7, N_BARS = 2 * STAGES + 8;
     static constexpr int TMEM_SLOT = 32 * 8;               // TMEM base word after 32 barrier slots
     static_assert(N_BARS <= 32, "barrier slots");
+    static_assert(RECV_OFF + RECV_BYTES <= BODY, "receive area inside the data region");
+    static_assert(HD == 256 ? TB_BYTES <= Q_BYTES : TB_OFF + TB_BYTES <= BODY, "transposition buffer");
     static constexpr int SMEM = BAR_OFF + 512 + 1024;      // barriers + TMEM word, + alignment slack
     // TMEM columns
     static constexpr int TM_O = 0;
@@ -97,20 +118,30 @@ __device__ __forceinline__ void record_timeout(unsigned* status, unsigned bit) {
     atomicOr(status, bit);
 }
 
+// Barrier over the two softmax warps that share TMEM lane quadrant q (named
+// barriers 1..4, 64 threads each).
+__device__ __forceinline__ void quad_bar_sync(int q) {
+    asm volatile("bar.sync %0, 64;" :: "r"(q + 1) : "memory");
+}
+
 template <int HD>
 __global__ void __launch_bounds__(kThreads, 1)
-attn_tc_kernel(const __grid_constant__ TcArgs a, const __grid_constant__ RopeTable tb,
-               const __grid_constant__ Maps mp) {
+attn_tc_kernel(const __grid_constant__ TcArgs a, const __grid_constant__ Maps mp) {
     using C = Cfg<HD>;
     constexpr int BN = C::BN;
+    constexpr int HB = BN / 2;                           // S columns per softmax half
+    constexpr int OH = HD / 2;                           // O columns per softmax half
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     unsigned char* sm = reinterpret_cast<unsigned char*>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     unsigned char* sQ = sm;
     unsigned char* sStage = sm + C::Q_BYTES;
-    float* sRedO = reinterpret_cast<float*>(sm);                                   // after the KV loop
-    float2* sRedML = reinterpret_cast<float2*>(sm + kRows * C::RED_STRIDE * 4);
-    float2* sCS = reinterpret_cast<float2*>(sm + C::DATA);                        // [16][128] (cos, sin)
-    float* sW = reinterpret_cast<float*>(sm + C::DATA);                           // merge weights (later)
+    float* sRecvO = reinterpret_cast<float*>(sm + C::RECV_OFF);                     // after the KV loop
+    float* sTB = reinterpret_cast<float*>(sm + C::TB_OFF);                          // [8 warps][32][36]
+    unsigned char* aux = sm + C::DATA;
+    float* sMaxX = reinterpret_cast<float*>(aux + C::AUX_MAXX);       // loop: [2][2][128] half-row maxima
+    float* sLX = reinterpret_cast<float*>(aux + C::AUX_LX);           // [2][128] half-row sums
+    float2* sML = reinterpret_cast<float2*>(aux + C::AUX_ML);         // [C][R] (m, l) from the cluster
+    float* sW = reinterpret_cast<float*>(aux + C::AUX_W);             // merge weights
     uint64_t* bars = reinterpret_cast<uint64_t*>(sm + C::BAR_OFF);
     uint32_t* sTmemBase = reinterpret_cast<uint32_t*>(sm + C::BAR_OFF + C::TMEM_SLOT);
     __shared__ int s_last;
@@ -141,6 +172,7 @@ attn_tc_kernel(const __grid_constant__ TcArgs a, const __grid_constant__ RopeTab
     auto sMask = [&](int s) { return sStage + s * C::STAGE_BYTES + 2 * C::K_BYTES; };
 
     // ---- set-up ------------------------------------------------------------
+    const int my_r0 = (int)rank * R;
     if (tid == 0) {
         for (int s = 0; s < C::STAGES; ++s) {
             mbar_init(bar(C::B_FULL + s), 1);
@@ -148,96 +180,59 @@ attn_tc_kernel(const __grid_constant__ TcArgs a, const __grid_constant__ RopeTab
         }
         mbar_init(bar(C::B_SFULL + 0), 1);
         mbar_init(bar(C::B_SFULL + 1), 1);
-        mbar_init(bar(C::B_PFULL + 0), 128);
-        mbar_init(bar(C::B_PFULL + 1), 128);
+        mbar_init(bar(C::B_PFULL + 0), kSmaxThreads);
+        mbar_init(bar(C::B_PFULL + 1), kSmaxThreads);
         mbar_init(bar(C::B_ODONE), 1);
         mbar_init(bar(C::B_QFULL), 1);
         mbar_init(bar(C::B_PROBE), 1);
         mbar_init(bar(C::B_MMADONE), 1);
         mbar_fence_init();
-        if (a.q16) mbar_expect_tx(bar(C::B_QFULL), C::Q_BYTES);
+        // the whole Q tile arrives by TMA (each CTA multicasts its slice)
+        mbar_expect_tx(bar(C::B_QFULL), (uint32_t)C::Q_BYTES);
         prefetch_tmap(&mp.k);
         prefetch_tmap(&mp.v);
     }
     if (warp == kMmaWarp) tmem_alloc(smem_addr(sTmemBase), kTmemCols);
     tc_fence_before();
-    cluster_sync();                     // barriers of every CTA initialised
+    cluster_sync();                     // #1: barriers of every CTA initialised and armed
     tc_fence_after();
     const uint32_t tbase = *sTmemBase;
 
+    // K/V/mask tiles need no Q: the first ones are requested before the prologue
+    const uint32_t mask_tx = a.has_mask ? (uint32_t)(BN / 64) * 128u * (uint32_t)a.n_tok : 0u;
+    auto issue_load = [&](int i) {
+        const int st = i % C::STAGES;
+        mbar_expect_tx(bar(C::B_FULL + st), 2u * C::K_BYTES + mask_tx);
+        const int j0 = (t0 + i) * BN;
+#pragma unroll
+        for (int b = 0; b < C::NB; ++b) {
+            tma_load_2d(smem_addr(sK(st) + b * C::KV_BOX), &mp.k, b * 64, j0, bar(C::B_FULL + st));
+            tma_load_2d(smem_addr(sV(st) + b * C::KV_BOX), &mp.v, b * 64, j0, bar(C::B_FULL + st));
+        }
+        if (a.has_mask) {
+#pragma unroll
+            for (int mb = 0; mb < BN / 64; ++mb)
+                tma_load_2d(smem_addr(sMask(st) + mb * C::MASK_BOX), &mp.mask, j0 + mb * 64, 0, bar(C::B_FULL + st));
+        }
+    };
+    const int n_pre = min(C::STAGES, n_my);
+    if (warp == kProdWarp && lane == 0)
+        for (int i = 0; i < n_pre; ++i) issue_load(i);
+
     // ---- prologue: the 128 Q rows as f16, SW128 K-major in every CTA --------
-    const int my_r0 = (int)rank * R;
-    if (a.q16) {
-        if (tid == 0) {
-            for (int b = 0; b < C::NB; ++b) {
-                const uint32_t dst = smem_addr(sQ + b * C::Q_BOX + my_r0 * 128);
-                if (CS == 1)
-                    tma_load_2d(dst, &mp.q16, b * 64, row0 + my_r0, bar(C::B_QFULL));
-                else
-                    tma_load_2d_mc(dst, &mp.q16, b * 64, row0 + my_r0, bar(C::B_QFULL),
-                                   (uint16_t)((1u << CS) - 1u));
-            }
+    // CTA rank c multicasts rows [c*R, (c+1)*R) to the cluster. When the rows
+    // come from the qkv_post grid launched just before this one (programmatic
+    // dependent launch), wait for that grid here: everything above overlapped it.
+    if (tid == 0) {
+        asm volatile("griddepcontrol.wait;" ::: "memory");
+        for (int b = 0; b < C::NB; ++b) {
+            const uint32_t dst = smem_addr(sQ + b * C::Q_BOX + my_r0 * 128);
+            if (CS == 1)
+                tma_load_2d(dst, &mp.q16, b * 64, row0 + my_r0, bar(C::B_QFULL));
+            else
+                tma_load_2d_mc(dst, &mp.q16, b * 64, row0 + my_r0, bar(C::B_QFULL), (uint16_t)((1u << CS) - 1u));
         }
-    } else {
-        // cos/sin of every (token, pair) the owned rows need; heads share them
-        const int r_beg = my_r0, r_end = min(my_r0 + R, rows_real);
-        if (r_beg < r_end) {
-            const int tk0 = (row0 + r_beg) / a.n_head, tk1 = (row0 + r_end - 1) / a.n_head;
-            const int ntk = tk1 - tk0 + 1;
-            for (int i = tid; i < ntk * tb.half; i += kThreads) {
-                const int tt = i / tb.half, pr = i - tt * tb.half;
-                float c, s;
-                rope_cs(__ldg(a.pos + tk0 + tt), tb.turns[pr], tb.mscale, c, s);
-                sCS[tt * kMaxPairs + pr] = make_float2(c, s);
-            }
-            __syncthreads();
-            constexpr int CH = HD / 8;
-            for (int i = tid; i < (r_end - r_beg) * CH; i += kThreads) {
-                const int rr = r_beg + i / CH, ch = i % CH;
-                const int r = row0 + rr;
-                const int t = r / a.n_head, h = r - t * a.n_head;
-                const float* x = a.q + (int64_t)t * a.q_tok_stride + (int64_t)h * HD;
-                const float2* cs = sCS + (t - tk0) * kMaxPairs;
-                uint32_t pk[4];
-#pragma unroll
-                for (int e = 0; e < 8; e += 2) {
-                    float y[2];
-#pragma unroll
-                    for (int u = 0; u < 2; ++u) {
-                        const int d = ch * 8 + e + u;
-                        if (d < tb.half) {
-                            const float2 v = cs[d];
-                            y[u] = rope_lo(x[d], x[d + tb.half], v.x, v.y, tb.q_scale);
-                        } else if (d < tb.n_dims) {
-                            const int p = d - tb.half;
-                            const float2 v = cs[p];
-                            y[u] = rope_hi(x[p], x[d], v.x, v.y, tb.q_scale);
-                        } else {
-                            y[u] = __fmul_rn(x[d], tb.q_scale);
-                        }
-                    }
-                    pk[e / 2] = pack_half2(y[0], y[1]);
-                }
-                const int b = ch >> 3, c8 = ch & 7;
-                const uint32_t dst = smem_addr(sQ + b * C::Q_BOX + (rr >> 3) * 1024 + (rr & 7) * 128 +
-                                               ((c8 ^ (rr & 7)) << 4));
-                const uint4 val = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-                for (int p = 0; p < CS; ++p) st_cluster_v4(map_rank(dst, (uint32_t)p), val);
-            }
-        }
-        // rows >= M of this tile are zero in every CTA
-        constexpr int CH = HD / 8;
-        for (int i = tid; i < (kRows - rows_real) * CH; i += kThreads) {
-            const int rr = rows_real + i / CH, ch = i % CH;
-            const int b = ch >> 3, c8 = ch & 7;
-            *reinterpret_cast<uint4*>(sQ + b * C::Q_BOX + (rr >> 3) * 1024 + (rr & 7) * 128 + ((c8 ^ (rr & 7)) << 4)) =
-                make_uint4(0, 0, 0, 0);
-        }
-        fence_proxy_async_cta();
-        fence_proxy_async_cluster();
     }
-    cluster_sync();                     // Q rows (fused path) visible cluster-wide
-    tc_fence_after();
 
     if (a.probe_iters && tid == 0) {
         // test hook: a bounded wait on a barrier nothing ever signals
@@ -245,26 +240,16 @@ attn_tc_kernel(const __grid_constant__ TcArgs a, const __grid_constant__ RopeTab
     }
 
     // ---- main phase ----------------------------------------------------------
-    float m_ref = -INFINITY, l_sum = 0.f;
+    const int qd = warp & 3, half = (warp >> 2) & 1;     // softmax: lane quadrant, column half
+    const int r = qd * 32 + lane;                        // softmax: row of the tile
+    const uint32_t lane_base = (uint32_t)(qd * 32) << 16;
+    const bool quad_active = row0 + qd * 32 < a.M;
+    float m_ref = -INFINITY, l_part = 0.f;
     if (warp == kProdWarp) {
         if (lane == 0) {
-            const uint32_t mask_tx = a.has_mask ? (uint32_t)(BN / 64) * 128u * (uint32_t)a.n_tok : 0u;
-            for (int i = 0; i < n_my; ++i) {
-                const int st = i % C::STAGES;
-                if (i >= C::STAGES) wait(bar(C::B_EMPTY + st), ((i / C::STAGES) - 1) & 1);
-                mbar_expect_tx(bar(C::B_FULL + st), 2u * C::K_BYTES + mask_tx);
-                const int j0 = (t0 + i) * BN;
-#pragma unroll
-                for (int b = 0; b < C::NB; ++b) {
-                    tma_load_2d(smem_addr(sK(st) + b * C::KV_BOX), &mp.k, b * 64, j0, bar(C::B_FULL + st));
-                    tma_load_2d(smem_addr(sV(st) + b * C::KV_BOX), &mp.v, b * 64, j0, bar(C::B_FULL + st));
-                }
-                if (a.has_mask) {
-#pragma unroll
-                    for (int mb = 0; mb < BN / 64; ++mb)
-                        tma_load_2d(smem_addr(sMask(st) + mb * C::MASK_BOX), &mp.mask, j0 + mb * 64, 0,
-                                    bar(C::B_FULL + st));
-                }
+            for (int i = n_pre; i < n_my; ++i) {
+                wait(bar(C::B_EMPTY + i % C::STAGES), ((i / C::STAGES) - 1) & 1);
+                issue_load(i);
             }
             // drain: every issued load has landed before the stage memory is reused
             // (full time limit even after a failure: no copy may outlive the CTA)
@@ -274,9 +259,9 @@ attn_tc_kernel(const __grid_constant__ TcArgs a, const __grid_constant__ RopeTab
         }
     } else if (warp == kMmaWarp) {
         if (lane == 0) {
-            // given f16 Q: every CTA's multicast slices must have landed (full limit:
-            // peers write this CTA's shared memory)
-            if (a.q16 && !mbar_wait(bar(C::B_QFULL), 0, limit)) record_timeout(a.status, 1u);
+            // the Q tile must have landed (full limit: other CTAs' multicasts
+            // write this CTA's shared memory)
+            if (!mbar_wait(bar(C::B_QFULL), 0, limit)) record_timeout(a.status, 1u);
             tc_fence_after();
             constexpr uint32_t idS = idesc_f16_f32(kRows, BN, 0, 0);
             constexpr uint32_t idO = idesc_f16_f32(kRows, HD, 0, 1);
@@ -306,8 +291,8 @@ attn_tc_kernel(const __grid_constant__ TcArgs a, const __grid_constant__ RopeTab
                 wait(bar(C::B_PFULL + (i & 1)), (i >> 1) & 1);
                 tc_fence_after();
                 const uint32_t v_base = smem_addr(sV(i % C::STAGES));
-                const uint32_t p_tm = tbase + C::TM_P + (i & 1) * (BN / 2);
-                const uint32_t pl_tm = tbase + C::TM_PL + (i & 1) * (BN / 2);
+                const uint32_t p_tm = tbase + C::TM_P + (i & 1) * HB;
+                const uint32_t pl_tm = tbase + C::TM_PL + (i & 1) * HB;
 #pragma unroll
                 for (int ks = 0; ks < BN / 16; ++ks) {
                     const uint64_t vd = sdesc_sw128(v_base + ks * 2048, C::KV_BOX, 1024);
@@ -323,28 +308,28 @@ attn_tc_kernel(const __grid_constant__ TcArgs a, const __grid_constant__ RopeTab
             if (!mbar_wait(bar(C::B_MMADONE), 0, limit)) record_timeout(a.status, 1u);
         }
     } else {
-        // softmax warps: thread `tid` owns row `tid` of the tile
-        const int r = tid;
+        // softmax: warps w and w+4 share TMEM lanes [32(w%4), +32) (row r); warp
+        // w < 4 takes S columns [0, BN/2), warp w+4 takes [BN/2, BN). The two
+        // halves of a row exchange their maxima through shared memory per tile.
         const int grow = row0 + r;
         const int t = grow < a.M ? grow / a.n_head : a.n_tok - 1;
-        const bool warp_active = row0 + warp * 32 < a.M;
-        const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+        const int c_base = half * HB;
         for (int i = 0; i < n_my; ++i) {
             wait(bar(C::B_SFULL + (i & 1)), (i >> 1) & 1);
             tc_fence_after();
-            if (warp_active) {
-                float x[BN];
-#pragma unroll
-                for (int c = 0; c < BN; c += 32)
-                    tmem_ld_x32(tbase + lane_base + C::TM_S + (i & 1) * BN + c, reinterpret_cast<uint32_t*>(x + c));
+            float x[HB];
+            float pm = -INFINITY;
+            const int j0 = (t0 + i) * BN + c_base;
+            if (quad_active) {
+                tmem_ld_x32(tbase + lane_base + C::TM_S + (i & 1) * BN + c_base, reinterpret_cast<uint32_t*>(x));
                 tmem_wait_ld();
-                const int j0 = (t0 + i) * BN;
-                const unsigned char* mk = sMask(i % C::STAGES);
                 const float kq = a.kq_log2;
                 if (a.has_mask) {
+                    const unsigned char* mk = sMask(i % C::STAGES);
 #pragma unroll
-                    for (int c8 = 0; c8 < BN / 8; ++c8) {
-                        const int mb = c8 >> 3, ch = c8 & 7;
+                    for (int c8 = 0; c8 < HB / 8; ++c8) {
+                        const int col = c_base + c8 * 8;
+                        const int mb = col >> 6, ch = (col & 63) >> 3;
                         const uint4 raw = *reinterpret_cast<const uint4*>(mk + mb * C::MASK_BOX + t * 128 +
                                                                          ((ch ^ (t & 7)) << 4));
                         const __half2* h2 = reinterpret_cast<const __half2*>(&raw);
@@ -357,56 +342,60 @@ attn_tc_kernel(const __grid_constant__ TcArgs a, const __grid_constant__ RopeTab
                     }
                 } else {
 #pragma unroll
-                    for (int c = 0; c < BN; ++c) x[c] *= kq;
+                    for (int c = 0; c < HB; ++c) x[c] *= kq;
                 }
-                if (j0 + BN > a.n_kv) {               // ragged last tile only
+                if (j0 + HB > a.n_kv) {               // ragged last tile only
 #pragma unroll
-                    for (int c = 0; c < BN; ++c)
+                    for (int c = 0; c < HB; ++c)
                         if (j0 + c >= a.n_kv) x[c] = -INFINITY;
                 }
-                float mx = -INFINITY;
+                float pm4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-                for (int c = 0; c < BN; ++c) mx = fmaxf(mx, x[c]);
-                float m_new = m_ref;
-                if (mx > m_ref + kTau || (m_ref == -INFINITY && mx > -INFINITY)) m_new = fmaxf(mx, m_ref);
-                const bool grow_ref = m_ref != -INFINITY && m_new != m_ref;
-                const float alpha = grow_ref ? ex2(m_ref - m_new) : 1.f;
+                for (int c = 0; c < HB; ++c) pm4[c & 3] = fmaxf(pm4[c & 3], x[c]);
+                pm = fmaxf(fmaxf(pm4[0], pm4[1]), fmaxf(pm4[2], pm4[3]));
+            }
+            sMaxX[((i & 1) * 2 + half) * kRows + r] = pm;
+            quad_bar_sync(qd);
+            const float mx = fmaxf(pm, sMaxX[((i & 1) * 2 + (half ^ 1)) * kRows + r]);
+            float m_new = m_ref;
+            if (mx > m_ref + kTau || (m_ref == -INFINITY && mx > -INFINITY)) m_new = fmaxf(mx, m_ref);
+            const bool grow_ref = m_ref != -INFINITY && m_new != m_ref;
+            const float alpha = grow_ref ? ex2(m_ref - m_new) : 1.f;
+            if (quad_active) {
                 if (__any_sync(0xffffffffu, grow_ref) && i > 0) {
-                    // O holds PV up to tile i-1: wait for it, then rescale this warp's rows
+                    // O holds PV up to tile i-1: wait for it, then rescale this half of the row
                     wait(bar(C::B_ODONE), (i - 1) & 1);
                     tc_fence_after();
 #pragma unroll 1
-                    for (int c = 0; c < HD; c += 32) {
+                    for (int c = 0; c < OH; c += 32) {
                         uint32_t o[32];
-                        tmem_ld_x32(tbase + lane_base + C::TM_O + c, o);
+                        tmem_ld_x32(tbase + lane_base + C::TM_O + half * OH + c, o);
                         tmem_wait_ld();
 #pragma unroll
                         for (int u = 0; u < 32; ++u) o[u] = __float_as_uint(__uint_as_float(o[u]) * alpha);
-                        tmem_st_x32(tbase + lane_base + C::TM_O + c, o);
+                        tmem_st_x32(tbase + lane_base + C::TM_O + half * OH + c, o);
                     }
                     tmem_wait_st();
                 }
-                m_ref = m_new;
-                const float m_sub = m_ref == -INFINITY ? 0.f : m_ref;
-                float sum = 0.f;
-                uint32_t pk[BN / 2], pl[BN / 2];
+                const float m_sub = m_new == -INFINITY ? 0.f : m_new;
+                float sum4[4] = {0.f, 0.f, 0.f, 0.f};
+                uint32_t pk[HB / 2], pl[HB / 2];
 #pragma unroll
-                for (int c = 0; c < BN; c += 2) {
+                for (int c = 0; c < HB; c += 2) {
                     const float p0 = ex2(x[c] - m_sub), p1 = ex2(x[c + 1] - m_sub);
-                    sum += p0 + p1;
-                    const uint32_t h = pack_half2(p0, p1);
-                    const float2 hf = __half22float2(*reinterpret_cast<const __half2*>(&h));
-                    pk[c / 2] = h;
+                    sum4[(c >> 1) & 3] += p0 + p1;
+                    const uint32_t hbits = pack_half2(p0, p1);
+                    const float2 hf = __half22float2(*reinterpret_cast<const __half2*>(&hbits));
+                    pk[c / 2] = hbits;
                     pl[c / 2] = pack_half2(p0 - hf.x, p1 - hf.y);
                 }
-                l_sum = fmaf(l_sum, alpha, sum);
-#pragma unroll
-                for (int c = 0; c < BN / 2; c += 32) {
-                    tmem_st_x32(tbase + lane_base + C::TM_P + (i & 1) * (BN / 2) + c, pk + c);
-                    tmem_st_x32(tbase + lane_base + C::TM_PL + (i & 1) * (BN / 2) + c, pl + c);
-                }
+                const float sum = (sum4[0] + sum4[1]) + (sum4[2] + sum4[3]);
+                l_part = fmaf(l_part, alpha, sum);
+                tmem_st_x16(tbase + lane_base + C::TM_P + (i & 1) * HB + half * (HB / 2), pk);
+                tmem_st_x16(tbase + lane_base + C::TM_PL + (i & 1) * HB + half * (HB / 2), pl);
                 tmem_wait_st();
             }
+            m_ref = m_new;
             tc_fence_before();
             mbar_arrive(bar(C::B_PFULL + (i & 1)));
         }
@@ -414,20 +403,26 @@ attn_tc_kernel(const __grid_constant__ TcArgs a, const __grid_constant__ RopeTab
             if (!mbar_wait(bar(C::B_ODONE), (n_my - 1) & 1, limit)) record_timeout(a.status, 1u);
             tc_fence_after();
         }
+        // the row sum is the sum of both halves' partial sums
+        sLX[half * kRows + r] = l_part;
+        quad_bar_sync(qd);
+        l_part += sLX[(half ^ 1) * kRows + r];
     }
     __syncthreads();                    // every async load drained, every MMA done
+    tc_fence_before();
+    cluster_sync();                     // #3: every CTA is done with its data region
 
-    // ---- stage this CTA's (m, l, O) for the cluster merge ------------------
-    if (warp < 4) {
-        const int r = tid;
-        const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
-        float* dst = sRedO + r * C::RED_STRIDE;
-        const bool have = n_my > 0 && row0 + warp * 32 < a.M;
+    // ---- push (m, l, O) rows to the CTA that owns them in this cluster ------
+    // rank c owns rows [c*R, (c+1)*R) of the tile: sML[src][row], sRecvO[src][row][RS]
+    if (warp < kSmaxWarps && quad_active) {
+        tc_fence_after();
+        float* tb_w = sTB + warp * (32 * 36);
+        const int srow = lane >> 3, scol = (lane & 7) * 4;   // 4 rows x 32 columns per step
 #pragma unroll 1
-        for (int c = 0; c < HD; c += 32) {
+        for (int c = 0; c < OH; c += 32) {
             uint32_t o[32];
-            if (have) {
-                tmem_ld_x32(tbase + lane_base + C::TM_O + c, o);
+            if (n_my > 0) {
+                tmem_ld_x32(tbase + lane_base + C::TM_O + half * OH + c, o);
                 tmem_wait_ld();
             } else {
 #pragma unroll
@@ -435,71 +430,80 @@ attn_tc_kernel(const __grid_constant__ TcArgs a, const __grid_constant__ RopeTab
             }
 #pragma unroll
             for (int u = 0; u < 32; u += 4)
-                *reinterpret_cast<uint4*>(dst + c + u) = make_uint4(o[u], o[u + 1], o[u + 2], o[u + 3]);
+                *reinterpret_cast<uint4*>(tb_w + lane * 36 + u) = make_uint4(o[u], o[u + 1], o[u + 2], o[u + 3]);
+            __syncwarp();
+#pragma unroll
+            for (int st = 0; st < 8; ++st) {
+                const int rr = qd * 32 + st * 4 + srow;          // tile row this lane stores
+                if (rr < rows_real) {
+                    const int ow = rr / R, olr = rr - ow * R;
+                    const uint4 v = *reinterpret_cast<const uint4*>(tb_w + (st * 4 + srow) * 36 + scol);
+                    st_cluster_v4(map_rank(smem_addr(sRecvO + ((int)rank * R + olr) * C::RS + half * OH + c + scol),
+                                           (uint32_t)ow), v);
+                }
+            }
+            __syncwarp();
         }
-        sRedML[r] = have ? make_float2(m_ref, l_sum) : make_float2(-INFINITY, 0.f);
+        if (half == 0 && r < rows_real) {
+            const int owner = r / R, lr = r - owner * R;
+            const float2 ml = n_my > 0 ? make_float2(m_ref, l_part) : make_float2(-INFINITY, 0.f);
+            const uint32_t dml = map_rank(smem_addr(sML + (int)rank * R + lr), (uint32_t)owner);
+            asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};" :: "r"(dml), "f"(ml.x), "f"(ml.y) : "memory");
+        }
     }
     tc_fence_before();
-    cluster_sync();                     // every CTA's staging complete
+    cluster_sync();                     // #4: every push has landed; no remote access after this
 
-    // ---- cluster merge of rows [rank*R, rank*R + R) -------------------------
+    // ---- merge the cluster's states for rows [rank*R, rank*R + R) ----------
     const int mr0 = (int)rank * R;
     const int mrows = max(0, min(R, rows_real - mr0));
     float* wts = sW;                         // [R][CS]
     float* rowM = sW + R * CS;               // [R]
     float* rowL = rowM + R;                  // [R]
     if (tid < mrows) {
-        const int rr = mr0 + tid;
-        float mv[8], lv[8];
         float mmax = -INFINITY;
-        for (int p = 0; p < CS; ++p) {
-            const float2 ml = ld_cluster_v2f(map_rank(smem_addr(sRedML + rr), (uint32_t)p));
-            mv[p] = ml.x;
-            lv[p] = ml.y;
-            mmax = fmaxf(mmax, ml.x);
-        }
+        for (int p = 0; p < CS; ++p) mmax = fmaxf(mmax, sML[p * R + tid].x);
         const float ref = mmax == -INFINITY ? 0.f : mmax;
         float L = 0.f;
         for (int p = 0; p < CS; ++p) {
-            const float w = mv[p] == -INFINITY ? 0.f : ex2(mv[p] - ref);
+            const float2 ml = sML[p * R + tid];
+            const float w = ml.x == -INFINITY ? 0.f : ex2(ml.x - ref);
             wts[tid * CS + p] = w;
-            L = fmaf(w, lv[p], L);
+            L = fmaf(w, ml.y, L);
         }
         rowM[tid] = mmax;
         rowL[tid] = L;
     }
     __syncthreads();
     const bool single = a.n_clusters == 1;
-    constexpr int Q4 = HD / 4;
-    for (int i = tid; i < mrows * Q4; i += kThreads) {
-        const int lr = i / Q4, q4 = i - lr * Q4;
-        const int rr = mr0 + lr;
-        const uint32_t src = smem_addr(sRedO + rr * C::RED_STRIDE + q4 * 4);
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int p = 0; p < CS; ++p) {
-            const float w = wts[lr * CS + p];
-            const float4 v = ld_cluster_v4f(map_rank(src, (uint32_t)p));
-            acc.x = fmaf(w, v.x, acc.x);
-            acc.y = fmaf(w, v.y, acc.y);
-            acc.z = fmaf(w, v.z, acc.z);
-            acc.w = fmaf(w, v.w, acc.w);
-        }
-        const int grow = row0 + rr;
-        if (single) {
-            const float L = rowL[lr];
-            float4 o;
-            o.x = L > 0.f ? acc.x / L : 0.f;
-            o.y = L > 0.f ? acc.y / L : 0.f;
-            o.z = L > 0.f ? acc.z / L : 0.f;
-            o.w = L > 0.f ? acc.w / L : 0.f;
-            *reinterpret_cast<float4*>(a.out + (int64_t)grow * HD + q4 * 4) = o;
-        } else {
-            const int64_t slot = ((int64_t)rt * a.n_clusters + cl) * kRows + rr;
-            *reinterpret_cast<float4*>(a.part_o + slot * HD + q4 * 4) = acc;
-            if (q4 == 0) a.part_ml[slot] = make_float2(rowM[lr], rowL[lr]);
+    {
+        constexpr int Q4 = HD / 4;
+        for (int i = tid; i < mrows * Q4; i += kThreads) {
+            const int lr = i / Q4, q4 = i - lr * Q4;
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int p = 0; p < CS; ++p) {            // rank order: deterministic
+                const float w = wts[lr * CS + p];
+                const float4 v = *reinterpret_cast<const float4*>(sRecvO + (p * R + lr) * C::RS + q4 * 4);
+                acc.x = fmaf(w, v.x, acc.x);
+                acc.y = fmaf(w, v.y, acc.y);
+                acc.z = fmaf(w, v.z, acc.z);
+                acc.w = fmaf(w, v.w, acc.w);
+            }
+            if (single) {
+                const float L = rowL[lr];
+                float4 o;
+                o.x = L > 0.f ? acc.x / L : 0.f;
+                o.y = L > 0.f ? acc.y / L : 0.f;
+                o.z = L > 0.f ? acc.z / L : 0.f;
+                o.w = L > 0.f ? acc.w / L : 0.f;
+                *reinterpret_cast<float4*>(a.out + (int64_t)(row0 + mr0 + lr) * HD + q4 * 4) = o;
+            } else {
+                const int64_t slot = ((int64_t)rt * a.n_clusters + cl) * kRows + mr0 + lr;
+                *reinterpret_cast<float4*>(a.part_o + slot * HD + q4 * 4) = acc;
+                if (q4 == 0) a.part_ml[slot] = make_float2(rowM[lr], rowL[lr]);
+            }
         }
     }
-    cluster_sync();                     // peers finished reading this CTA's staging
 
     // ---- merge across clusters: the last CTA of each (row tile, rank) slice ---
     if (!single) {
@@ -515,15 +519,19 @@ attn_tc_kernel(const __grid_constant__ TcArgs a, const __grid_constant__ RopeTab
             const int NC = a.n_clusters;
             float* w2 = sW;                          // [R][NC]
             float* L2 = sW + R * NC;                 // [R]
+            float2* ml2 = reinterpret_cast<float2*>(sRecvO);      // [R][NC] (m, l), local scratch
+            for (int i = tid; i < mrows * NC; i += kThreads) {    // every (row, cluster) at once
+                const int lr = i / NC, c2 = i - lr * NC;
+                ml2[i] = __ldcg(a.part_ml + ((int64_t)rt * NC + c2) * kRows + mr0 + lr);
+            }
+            __syncthreads();
             if (tid < mrows) {
-                const int rr = mr0 + tid;
                 float mmax = -INFINITY;
-                for (int c2 = 0; c2 < NC; ++c2)
-                    mmax = fmaxf(mmax, __ldcg(a.part_ml + ((int64_t)rt * NC + c2) * kRows + rr).x);
+                for (int c2 = 0; c2 < NC; ++c2) mmax = fmaxf(mmax, ml2[tid * NC + c2].x);
                 const float ref = mmax == -INFINITY ? 0.f : mmax;
                 float L = 0.f;
                 for (int c2 = 0; c2 < NC; ++c2) {
-                    const float2 ml = __ldcg(a.part_ml + ((int64_t)rt * NC + c2) * kRows + rr);
+                    const float2 ml = ml2[tid * NC + c2];
                     const float w = ml.x == -INFINITY ? 0.f : ex2(ml.x - ref);
                     w2[tid * NC + c2] = w;
                     L = fmaf(w, ml.y, L);
@@ -531,18 +539,27 @@ attn_tc_kernel(const __grid_constant__ TcArgs a, const __grid_constant__ RopeTab
                 L2[tid] = L;
             }
             __syncthreads();
+            constexpr int Q4 = HD / 4;
             for (int i = tid; i < mrows * Q4; i += kThreads) {
                 const int lr = i / Q4, q4 = i - lr * Q4;
                 const int rr = mr0 + lr;
+                const float* src = a.part_o + (((int64_t)rt * NC) * kRows + rr) * HD + q4 * 4;
+                const int64_t cstride = (int64_t)kRows * HD;
                 float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-                for (int c2 = 0; c2 < NC; ++c2) {
-                    const float w = w2[lr * NC + c2];
-                    const float4 v = __ldcg(reinterpret_cast<const float4*>(
-                        a.part_o + (((int64_t)rt * NC + c2) * kRows + rr) * HD + q4 * 4));
-                    acc.x = fmaf(w, v.x, acc.x);
-                    acc.y = fmaf(w, v.y, acc.y);
-                    acc.z = fmaf(w, v.z, acc.z);
-                    acc.w = fmaf(w, v.w, acc.w);
+                for (int c0 = 0; c0 < NC; c0 += 8) {
+                    float4 v[8];
+#pragma unroll
+                    for (int u = 0; u < 8; ++u)          // eight independent loads in flight
+                        v[u] = c0 + u < NC ? __ldcg(reinterpret_cast<const float4*>(src + (c0 + u) * cstride))
+                                           : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) {
+                        const float w = c0 + u < NC ? w2[lr * NC + c0 + u] : 0.f;
+                        acc.x = fmaf(w, v[u].x, acc.x);
+                        acc.y = fmaf(w, v[u].y, acc.y);
+                        acc.z = fmaf(w, v[u].z, acc.z);
+                        acc.w = fmaf(w, v[u].w, acc.w);
+                    }
                 }
                 const float L = L2[lr];
                 float4 o;
@@ -617,7 +634,7 @@ static fr_status launch(const TcLaunch& L, cudaStream_t stream) {
     if (!encode_2d(&mp.k, L.k, HD, a.n_kv, L.k_rs, 64, BN)) return FR_ERR_CUDA;
     if (!encode_2d(&mp.v, L.v, HD, a.n_kv, L.v_rs, 64, BN)) return FR_ERR_CUDA;
     if (a.has_mask && !encode_2d(&mp.mask, L.mask, a.n_kv, a.n_tok, L.m_rs, 64, a.n_tok)) return FR_ERR_CUDA;
-    if (a.q16 && !encode_2d(&mp.q16, a.q16, HD, a.M, HD, 64, kRows / a.C)) return FR_ERR_CUDA;
+    if (!a.q16 || !encode_2d(&mp.q16, a.q16, HD, a.M, HD, 64, kRows / a.C)) return FR_ERR_CUDA;
 
     cudaLaunchConfig_t cfg;
     memset(&cfg, 0, sizeof(cfg));
@@ -625,14 +642,16 @@ static fr_status launch(const TcLaunch& L, cudaStream_t stream) {
     cfg.blockDim = dim3(kThreads, 1, 1);
     cfg.dynamicSmemBytes = Cfg<HD>::SMEM;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = 1;
     attr[0].val.clusterDim.y = a.C;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, attn_tc_kernel<HD>, a, L.tb, mp);
+    cfg.numAttrs = L.pdl ? 2 : 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, attn_tc_kernel<HD>, a, mp);
     return e == cudaSuccess ? FR_OK : FR_ERR_CUDA;
 }
 

@@ -33,6 +33,11 @@ struct RopeTable {
 // Host: validate the parameters and fill the table. Returns false if invalid.
 bool build_rope_table(const fr_rope_params* rp, float q_scale, int hd, RopeTable* t);
 
+// Host: enqueue the qkv_post kernel (arguments already validated). The kernel
+// lets a programmatically dependent launch start early.
+fr_status launch_qkv_post(const float* q, int64_t q_tok_stride, const int32_t* pos, int n_tok, int n_head,
+                          int hd, const RopeTable& tb, uint16_t* q16_out, float* q32_out, cudaStream_t stream);
+
 // Scaled cosine and sine of pair i at integer position pos.
 __device__ __forceinline__ void rope_cs(int pos, uint64_t turns, float mscale, float& c, float& s) {
     const uint64_t a = (uint64_t)(int64_t)pos * turns;      // mod 2^64 = mod one turn

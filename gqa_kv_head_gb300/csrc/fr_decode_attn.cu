@@ -382,10 +382,14 @@ static size_t v1_workspace_bytes(int M, int hd, int n_kv) {
     return kWsHeader + splits * M * hd * sizeof(float) + splits * M * sizeof(float2);
 }
 
+// Tensor-core kernel workspace: [header][f16 Q rows handed from qkv_post]
+// [cluster partial O][cluster partial (m, l)].
+static size_t tc_q16_bytes(int M, int hd) { return ((size_t)M * hd * 2 + 1023) & ~(size_t)1023; }
+
 static size_t tc_workspace_bytes(int M, int hd) {
     const size_t row_tiles = (size_t)(M + 127) / 128;
     const size_t slots = row_tiles * tc::kMaxClusters * 128;
-    return kWsHeader + slots * hd * sizeof(float) + slots * sizeof(float2);
+    return kWsHeader + tc_q16_bytes(M, hd) + slots * hd * sizeof(float) + slots * sizeof(float2);
 }
 
 static size_t workspace_bytes_for(int M, int hd, int n_kv) {
@@ -405,14 +409,20 @@ static TcPlan make_tc_plan(int M, int hd, int n_kv, int num_sms, int force_split
     const int bn = tc::tile_keys(hd);
     p.row_tiles = (M + 127) / 128;
     p.n_tiles = (n_kv + bn - 1) / bn;
-    int C = force_cluster > 0 ? force_cluster : 8;
+    // clusters of 8 for one row tile; with several row tiles (whose CTAs share
+    // each K/V tile through L2) clusters of 4, which fit more CTAs per GPU
+    int C = force_cluster > 0 ? force_cluster : (p.row_tiles > 1 ? 4 : 8);
     while (C > 1 && C > p.n_tiles) C >>= 1;
     int n_cl;
     if (force_splits > 0) {
         n_cl = (force_splits + C - 1) / C;
     } else {
+        // co-resident CTAs at one CTA per SM for this cluster size
         const int budget = C >= 8 ? (num_sms * 120) / 152 : (C == 4 ? (num_sms * 144) / 152 : num_sms);
         n_cl = budget / (p.row_tiles * C);
+        // at least two KV tiles per CTA: below that the merge costs more than
+        // the extra streaming
+        n_cl = min(n_cl, (p.n_tiles + 2 * C - 1) / (2 * C));
     }
     n_cl = max(1, min(n_cl, min(tc::kMaxClusters, (p.n_tiles + C - 1) / C)));
     int S = C * n_cl;
@@ -491,15 +501,23 @@ static fr_status decode_attn_impl(const uint16_t* q16, const float* q, int64_t q
         tc::TcLaunch L;
         memset(&L, 0, sizeof(L));
         tc::TcArgs& a = L.args;
-        a.q16 = reinterpret_cast<const __half*>(q16);
-        a.q = q;
-        a.q_tok_stride = q_tok_stride;
-        a.pos = pos;
+        unsigned char* qslot = w + kWsHeader;
+        unsigned char* parts = qslot + tc_q16_bytes(M, hd);
+        if (q16) {
+            a.q16 = reinterpret_cast<const __half*>(q16);
+        } else {
+            // qkv_post hands its f16 rows to the attention through the workspace
+            const fr_status st = launch_qkv_post(q, q_tok_stride, pos, n_tok, n_head, hd, tb,
+                                                 reinterpret_cast<uint16_t*>(qslot), nullptr, stream);
+            if (st != FR_OK) return st;
+            a.q16 = reinterpret_cast<const __half*>(qslot);
+            L.pdl = true;
+        }
         a.out = out;
         a.status = reinterpret_cast<unsigned*>(w);
         a.tickets = reinterpret_cast<unsigned*>(w + kWsTickets);
-        a.part_o = reinterpret_cast<float*>(w + kWsHeader);
-        a.part_ml = reinterpret_cast<float2*>(w + kWsHeader + slots * hd * sizeof(float));
+        a.part_o = reinterpret_cast<float*>(parts);
+        a.part_ml = reinterpret_cast<float2*>(parts + slots * hd * sizeof(float));
         a.has_mask = mask != nullptr;
         a.n_tok = n_tok;
         a.n_head = n_head;
@@ -512,7 +530,6 @@ static fr_status decode_attn_impl(const uint16_t* q16, const float* q, int64_t q
         a.kq_log2 = kq_scale * kLog2e;
         a.wait_limit_ns = tc::kWaitLimitNs;
         a.probe_iters = (uint32_t)o.wait_probe_iters;
-        L.tb = tb;
         L.k = k;
         L.v = v;
         L.mask = mask;

@@ -73,6 +73,9 @@ __global__ void __launch_bounds__(256)
 qkv_post_kernel(const float* __restrict__ q, int64_t q_tok_stride, const int32_t* __restrict__ pos,
                 int n_head, int M, __half* __restrict__ q16, float* __restrict__ q32,
                 const __grid_constant__ RopeTable tb) {
+    // a dependent attention launch may start its set-up and K/V loads now; it
+    // waits for this grid's completion before it reads the rows
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int r = blockIdx.x * blockDim.y + threadIdx.y;
     if (r >= M) return;
     const int c = threadIdx.x;                 // slot 0 .. HD/2-1
@@ -89,6 +92,22 @@ qkv_post_kernel(const float* __restrict__ q, int64_t q_tok_stride, const int32_t
         frow[d0] = y0;
         frow[d1] = y1;
     }
+}
+
+fr_status launch_qkv_post(const float* q, int64_t q_tok_stride, const int32_t* pos, int n_tok, int n_head,
+                          int hd, const RopeTable& tb, uint16_t* q16_out, float* q32_out, cudaStream_t stream) {
+    const int M = n_tok * n_head;
+    const int slots = hd / 2;
+    const int rows_per_block = 256 / slots;
+    dim3 block(slots, rows_per_block);
+    dim3 grid((M + rows_per_block - 1) / rows_per_block);
+    __half* o16 = reinterpret_cast<__half*>(q16_out);
+    switch (hd) {
+        case 64: qkv_post_kernel<64><<<grid, block, 0, stream>>>(q, q_tok_stride, pos, n_head, M, o16, q32_out, tb); break;
+        case 128: qkv_post_kernel<128><<<grid, block, 0, stream>>>(q, q_tok_stride, pos, n_head, M, o16, q32_out, tb); break;
+        default: qkv_post_kernel<256><<<grid, block, 0, stream>>>(q, q_tok_stride, pos, n_head, M, o16, q32_out, tb); break;
+    }
+    return cudaGetLastError() == cudaSuccess ? FR_OK : FR_ERR_CUDA;
 }
 
 }  // namespace fr
@@ -122,16 +141,5 @@ extern "C" fr_status fr_qkv_post(const float* q, int64_t q_tok_stride, const int
         return FR_ERR_INVALID_ARG;
     RopeTable tb;
     if (!build_rope_table(rp, q_scale, hd, &tb)) return FR_ERR_INVALID_ARG;
-    const int M = n_tok * n_head;
-    const int slots = hd / 2;
-    const int rows_per_block = 256 / slots;
-    dim3 block(slots, rows_per_block);
-    dim3 grid((M + rows_per_block - 1) / rows_per_block);
-    __half* o16 = reinterpret_cast<__half*>(q16_out);
-    switch (hd) {
-        case 64: qkv_post_kernel<64><<<grid, block, 0, stream>>>(q, q_tok_stride, pos, n_head, M, o16, q32_out, tb); break;
-        case 128: qkv_post_kernel<128><<<grid, block, 0, stream>>>(q, q_tok_stride, pos, n_head, M, o16, q32_out, tb); break;
-        default: qkv_post_kernel<256><<<grid, block, 0, stream>>>(q, q_tok_stride, pos, n_head, M, o16, q32_out, tb); break;
-    }
-    return cudaGetLastError() == cudaSuccess ? FR_OK : FR_ERR_CUDA;
+    return launch_qkv_post(q, q_tok_stride, pos, n_tok, n_head, hd, tb, q16_out, q32_out, stream);
 }

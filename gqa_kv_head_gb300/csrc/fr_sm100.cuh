@@ -74,6 +74,16 @@ __device__ __forceinline__ void tma_load_2d_mc(uint32_t dst, const CUtensorMap* 
         " [%0], [%1, {%2, %3}], [%4], %5;"
         :: "r"(dst), "l"((uint64_t)map), "r"(x), "r"(y), "r"(bar), "h"(cta_mask) : "memory");
 }
+// Bulk copy of `bytes` (multiple of 16) from this CTA's shared memory to the
+// shared memory of a CTA in the cluster (dst and bar are shared::cluster
+// addresses from map_rank); the receiver's barrier is credited with the bytes.
+__device__ __forceinline__ void bulk_copy_to_peer(uint32_t dst, uint32_t src, uint32_t bytes, uint32_t bar) {
+    asm volatile("cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                 :: "r"(dst), "r"(src), "r"(bytes), "r"(bar) : "memory");
+}
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+    asm volatile("prefetch.global.L2 [%0];" :: "l"(p));
+}
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {
     asm volatile("prefetch.tensormap [%0];" :: "l"((uint64_t)map) : "memory");
 }
