@@ -28,7 +28,8 @@ class FrRopeParams(ctypes.Structure):
 
 class FrAttnOpts(ctypes.Structure):
     _fields_ = [("engine", ctypes.c_int), ("force_splits", ctypes.c_int),
-                ("force_cluster", ctypes.c_int), ("wait_probe_iters", ctypes.c_int)]
+                ("force_cluster", ctypes.c_int), ("wait_probe_iters", ctypes.c_int),
+                ("merge_mode", ctypes.c_int)]
 
 
 _P = ctypes.c_void_p

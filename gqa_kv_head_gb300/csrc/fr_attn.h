@@ -11,13 +11,14 @@ namespace fr {
 namespace tc {
 
 constexpr int kMaxClusters = 24;         // clusters per 128-row tile (workspace bound)
+constexpr int kMaxMergeSplits = 160;     // splits (over all row tiles) in merge-kernel mode
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // a wait gives up after ~2 s
 
 struct TcArgs {
     const __half* q16;        // f16 Q rows [M][hd] (given, or qkv_post's output)
     float* out;
-    float* part_o;            // [row_tiles][n_clusters][128][hd]
-    float2* part_ml;          // [row_tiles][n_clusters][128]
+    float* part_o;            // [row_tiles][n_clusters][128][hd]  (merge-kernel mode: [row_tiles][splits][128][hd])
+    float2* part_ml;          // [row_tiles][n_clusters][128]      (merge-kernel mode: [row_tiles][splits][128])
     unsigned* tickets;        // [row_tiles][C]
     unsigned* status;
     int has_mask;
@@ -26,6 +27,8 @@ struct TcArgs {
     int tiles_per_split;
     int n_clusters;           // clusters per row tile
     int C;                    // CTAs per cluster (splits per cluster)
+    int merge_kernel;         // 1: write every split's state for attn_merge_kernel (C == 1)
+    int splits;               // splits per row tile
     float kq_log2;
     uint64_t wait_limit_ns;
     uint32_t probe_iters;
@@ -43,6 +46,14 @@ struct TcLaunch {
 
 int tile_keys(int hd);
 fr_status launch_tc(const TcLaunch& L, int hd, cudaStream_t stream);
+// Merge of the split states written in merge-kernel mode (programmatic
+// dependent launch after the attention grid).
+fr_status launch_merge(const float* part_o, const float2* part_ml, float* out, int M, int splits, int hd,
+                       cudaStream_t stream);
 
 }  // namespace tc
+
+// Smallest workspace fr_decode_attn accepts for this shape (0 if unsupported);
+// fr_decode_attn_workspace_size may ask for more so that faster plans fit.
+size_t decode_attn_min_workspace_bytes(int n_tok, int n_head, int hd, int n_kv);
 }  // namespace fr

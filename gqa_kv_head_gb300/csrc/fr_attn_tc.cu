@@ -35,6 +35,10 @@
 //              tile the merged slices go to the workspace and the last CTA to
 //              arrive for each (row tile, rank) slice merges them (atomic ticket,
 //              reset afterwards). No CTA ever waits for another cluster.
+// Merge-kernel mode, for plans with many splits: no clusters, up to one split
+// per SM; each CTA writes its unnormalised (m, l, O) rows to the workspace and
+// attn_merge_kernel, chained by programmatic dependent launch, combines them
+// with the whole GPU instead of one CTA per slice.
 // Every mbarrier wait is bounded; a wait that gives up sets the workspace's
 // status word and the CTA still runs through every cluster barrier, drains
 // its copies and frees its TMEM.
@@ -197,6 +201,9 @@ attn_tc_kernel(const __grid_constant__ TcArgs a, const __grid_constant__ Maps mp
     cluster_sync();                     // #1: barriers of every CTA initialised and armed
     tc_fence_after();
     const uint32_t tbase = *sTmemBase;
+    // a dependent merge grid (merge-kernel mode) may be scheduled now; it waits
+    // for this grid's completion before reading the split states
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
     // K/V/mask tiles need no Q: the first ones are requested before the prologue
     const uint32_t mask_tx = a.has_mask ? (uint32_t)(BN / 64) * 128u * (uint32_t)a.n_tok : 0u;
@@ -412,6 +419,42 @@ attn_tc_kernel(const __grid_constant__ TcArgs a, const __grid_constant__ Maps mp
     tc_fence_before();
     cluster_sync();                     // #3: every CTA is done with its data region
 
+    if (a.merge_kernel) {
+        // ---- merge-kernel mode: this split's (m, l, O) rows go to the workspace
+        // (coalesced through the transposition buffer); attn_merge_kernel merges them
+        if (warp < kSmaxWarps && quad_active) {
+            tc_fence_after();
+            float* tb_w = sTB + warp * (32 * 36);
+            const int srow = lane >> 3, scol = (lane & 7) * 4;
+            float* base = a.part_o + ((int64_t)(rt * a.splits + split) * kRows) * HD + half * OH;
+#pragma unroll 1
+            for (int c = 0; c < OH; c += 32) {
+                uint32_t o[32];
+                if (n_my > 0) {
+                    tmem_ld_x32(tbase + lane_base + C::TM_O + half * OH + c, o);
+                    tmem_wait_ld();
+                } else {
+#pragma unroll
+                    for (int u = 0; u < 32; ++u) o[u] = 0u;
+                }
+#pragma unroll
+                for (int u = 0; u < 32; u += 4)
+                    *reinterpret_cast<uint4*>(tb_w + lane * 36 + u) = make_uint4(o[u], o[u + 1], o[u + 2], o[u + 3]);
+                __syncwarp();
+#pragma unroll
+                for (int st = 0; st < 8; ++st) {
+                    const int rr = qd * 32 + st * 4 + srow;
+                    if (rr < rows_real)
+                        *reinterpret_cast<uint4*>(base + (int64_t)rr * HD + c + scol) =
+                            *reinterpret_cast<const uint4*>(tb_w + (st * 4 + srow) * 36 + scol);
+                }
+                __syncwarp();
+            }
+            if (half == 0 && r < rows_real)
+                a.part_ml[(int64_t)(rt * a.splits + split) * kRows + r] =
+                    n_my > 0 ? make_float2(m_ref, l_part) : make_float2(-INFINITY, 0.f);
+        }
+    } else {
     // ---- push (m, l, O) rows to the CTA that owns them in this cluster ------
     // rank c owns rows [c*R, (c+1)*R) of the tile: sML[src][row], sRecvO[src][row][RS]
     if (warp < kSmaxWarps && quad_active) {
@@ -573,6 +616,8 @@ attn_tc_kernel(const __grid_constant__ TcArgs a, const __grid_constant__ Maps mp
         }
     }
 
+    }   // in-kernel merge
+
     // ---- teardown --------------------------------------------------------------
     tc_fence_before();
     __syncthreads();
@@ -581,6 +626,104 @@ attn_tc_kernel(const __grid_constant__ TcArgs a, const __grid_constant__ Maps mp
         tc_fence_after();
         tmem_dealloc(tbase, kTmemCols);
     }
+}
+
+// Merge of the split states written in merge-kernel mode. One CTA per (row,
+// 128-column chunk): the split weights 2^(m_s - max m) and the row sum first,
+// then 8 warps each add a fixed subset of the splits (in order) and the warps'
+// sums are added in order: the result does not depend on timing.
+template <int HD>
+__global__ void __launch_bounds__(256)
+attn_merge_kernel(const float* __restrict__ part_o, const float2* __restrict__ part_ml, float* __restrict__ out,
+                  int M, int splits) {
+    constexpr int CWM = HD < 128 ? HD : 128;
+    constexpr int NCH = HD / CWM;
+    constexpr int LANES = CWM / 4;
+    __shared__ float s_m[kMaxMergeSplits], s_w[kMaxMergeSplits], s_l[kMaxMergeSplits];
+    __shared__ float s_red[8][CWM];
+    __shared__ float s_max[8], s_sum[8];
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int row = blockIdx.x / NCH, chunk = blockIdx.x - row * NCH;
+    const int rt = row >> 7, rr = row & 127;
+    asm volatile("griddepcontrol.wait;" ::: "memory");     // the attention grid is complete
+    const float2* ml = part_ml + (int64_t)rt * splits * kRows + rr;
+    float mx = -INFINITY;
+    for (int s2 = tid; s2 < splits; s2 += 256) {
+        const float2 v = __ldcg(ml + (int64_t)s2 * kRows);
+        s_m[s2] = v.x;
+        s_l[s2] = v.y;
+        mx = fmaxf(mx, v.x);
+    }
+    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    if (lane == 0) s_max[warp] = mx;
+    __syncthreads();
+    mx = s_max[0];
+    for (int w = 1; w < 8; ++w) mx = fmaxf(mx, s_max[w]);
+    const float ref = mx == -INFINITY ? 0.f : mx;
+    float lsum = 0.f;
+    for (int s2 = tid; s2 < splits; s2 += 256) {
+        const float w = s_m[s2] == -INFINITY ? 0.f : ex2(s_m[s2] - ref);
+        s_w[s2] = w;
+        lsum = fmaf(w, s_l[s2], lsum);
+    }
+    for (int o = 16; o > 0; o >>= 1) lsum += __shfl_xor_sync(0xffffffffu, lsum, o);
+    if (lane == 0) s_sum[warp] = lsum;
+    __syncthreads();
+    float L = 0.f;
+    for (int w = 0; w < 8; ++w) L += s_sum[w];
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (lane < LANES) {
+        const float* base = part_o + ((int64_t)rt * splits * kRows + rr) * HD + chunk * CWM + lane * 4;
+        const int64_t sstride = (int64_t)kRows * HD;
+        for (int s0 = warp; s0 < splits; s0 += 8 * 4) {
+            float4 v[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {               // four independent loads in flight
+                const int s2 = s0 + 8 * u;
+                v[u] = s2 < splits ? __ldcg(reinterpret_cast<const float4*>(base + s2 * sstride))
+                                   : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int s2 = s0 + 8 * u;
+                const float w = s2 < splits ? s_w[s2] : 0.f;
+                acc.x = fmaf(w, v[u].x, acc.x);
+                acc.y = fmaf(w, v[u].y, acc.y);
+                acc.z = fmaf(w, v[u].z, acc.z);
+                acc.w = fmaf(w, v[u].w, acc.w);
+            }
+        }
+        *reinterpret_cast<float4*>(&s_red[warp][lane * 4]) = acc;
+    }
+    __syncthreads();
+    if (tid < CWM && row < M) {
+        float sum = 0.f;
+        for (int w = 0; w < 8; ++w) sum += s_red[w][tid];
+        out[(int64_t)row * HD + chunk * CWM + tid] = L > 0.f ? sum / L : 0.f;
+    }
+}
+
+fr_status launch_merge(const float* part_o, const float2* part_ml, float* out, int M, int splits, int hd,
+                       cudaStream_t stream) {
+    if (splits < 1 || splits > kMaxMergeSplits) return FR_ERR_UNSUPPORTED;
+    cudaLaunchConfig_t cfg;
+    memset(&cfg, 0, sizeof(cfg));
+    const int nch = hd < 128 ? 1 : hd / 128;
+    cfg.gridDim = dim3(M * nch, 1, 1);
+    cfg.blockDim = dim3(256, 1, 1);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e;
+    switch (hd) {
+        case 64: e = cudaLaunchKernelEx(&cfg, attn_merge_kernel<64>, part_o, part_ml, out, M, splits); break;
+        case 128: e = cudaLaunchKernelEx(&cfg, attn_merge_kernel<128>, part_o, part_ml, out, M, splits); break;
+        default: e = cudaLaunchKernelEx(&cfg, attn_merge_kernel<256>, part_o, part_ml, out, M, splits); break;
+    }
+    return e == cudaSuccess ? FR_OK : FR_ERR_CUDA;
 }
 
 // ---- host side ----------------------------------------------------------------

@@ -392,6 +392,14 @@ static size_t tc_workspace_bytes(int M, int hd) {
     return kWsHeader + tc_q16_bytes(M, hd) + slots * hd * sizeof(float) + slots * sizeof(float2);
 }
 
+// merge-kernel mode: [header][f16 Q rows][split O [row_tiles][splits][128][hd]][split (m, l)]
+static size_t tc_merge_workspace_bytes(int M, int hd) {
+    const size_t row_tiles = (size_t)(M + 127) / 128;
+    const size_t slots = row_tiles * ((tc::kMaxMergeSplits + row_tiles - 1) / row_tiles) * 128;
+    return kWsHeader + tc_q16_bytes(M, hd) + slots * hd * sizeof(float) + slots * sizeof(float2);
+}
+
+// Smallest workspace any plan of this shape accepts (in-kernel merge).
 static size_t workspace_bytes_for(int M, int hd, int n_kv) {
     const size_t a = v1_workspace_bytes(M, hd, n_kv), b = tc_workspace_bytes(M, hd);
     return a > b ? a : b;
@@ -402,6 +410,7 @@ static size_t workspace_bytes_for(int M, int hd, int n_kv) {
 // CTAs as are co-resident for that cluster size (1 CTA per SM).
 struct TcPlan {
     int row_tiles, n_tiles, C, n_clusters, splits, tiles_per_split;
+    int merge_kernel;      // 1: separate merge kernel (C == 1, splits over the whole GPU)
 };
 
 static TcPlan make_tc_plan(int M, int hd, int n_kv, int num_sms, int force_splits, int force_cluster) {
@@ -433,6 +442,35 @@ static TcPlan make_tc_plan(int M, int hd, int n_kv, int num_sms, int force_split
     p.C = C;
     p.n_clusters = n_cl;
     p.splits = C * n_cl;
+    p.merge_kernel = 0;
+    return p;
+}
+
+// Many splits make the in-kernel merge's serial tail dominate; then every SM
+// takes one split without clusters and a separate merge kernel reduces the
+// states with the whole GPU. Chosen when the cluster plan needs more than 4
+// clusters per row tile and the workspace holds the split states.
+static TcPlan choose_tc_plan(int M, int hd, int n_kv, int num_sms, const fr_attn_opts& o, size_t ws_bytes,
+                             bool* ok) {
+    TcPlan p = make_tc_plan(M, hd, n_kv, num_sms, o.force_splits, o.force_cluster);
+    *ok = true;
+    const bool fits = ws_bytes >= tc_merge_workspace_bytes(M, hd);
+    bool use = false;
+    if (o.merge_mode == 2) {
+        use = true;
+        if (!fits) *ok = false;
+    } else if (o.merge_mode == 0 && o.force_cluster == 0) {
+        use = p.n_clusters > 4 && fits;
+    }
+    if (!use) return p;
+    const int cap = tc::kMaxMergeSplits / p.row_tiles;
+    int S = o.force_splits > 0 ? o.force_splits : max(1, num_sms / p.row_tiles);
+    S = max(1, min(S, min(cap, o.force_splits > 0 ? p.n_tiles : (p.n_tiles + 1) / 2)));
+    p.tiles_per_split = (p.n_tiles + S - 1) / S;
+    p.splits = (p.n_tiles + p.tiles_per_split - 1) / p.tiles_per_split;
+    p.C = 1;
+    p.n_clusters = p.splits;
+    p.merge_kernel = 1;
     return p;
 }
 
@@ -462,9 +500,11 @@ static fr_status decode_attn_impl(const uint16_t* q16, const float* q, int64_t q
                                   const uint16_t* mask, int64_t m_rs, int n_tok, int n_head, int hd,
                                   int n_kv, float kq_scale, float* out, void* ws, size_t ws_bytes,
                                   const fr_attn_opts* opts, cudaStream_t stream) {
-    fr_attn_opts o = {0, 0, 0, 0};
+    fr_attn_opts o;
+    memset(&o, 0, sizeof(o));
     if (opts) o = *opts;
     if (o.engine < 0 || o.engine > 1 || o.force_splits < 0 || o.wait_probe_iters < 0) return FR_ERR_INVALID_ARG;
+    if (o.merge_mode < 0 || o.merge_mode > 2) return FR_ERR_INVALID_ARG;
     if (o.force_cluster != 0 && o.force_cluster != 1 && o.force_cluster != 2 && o.force_cluster != 4 &&
         o.force_cluster != 8)
         return FR_ERR_INVALID_ARG;
@@ -496,8 +536,10 @@ static fr_status decode_attn_impl(const uint16_t* q16, const float* q, int64_t q
     unsigned char* w = static_cast<unsigned char*>(ws);
 
     if (o.engine == 0) {
-        const TcPlan p = make_tc_plan(M, hd, n_kv, sms, o.force_splits, o.force_cluster);
-        const size_t slots = (size_t)p.row_tiles * p.n_clusters * 128;
+        bool plan_ok = true;
+        const TcPlan p = choose_tc_plan(M, hd, n_kv, sms, o, ws_bytes, &plan_ok);
+        if (!plan_ok) return FR_ERR_WORKSPACE;
+        const size_t slots = (size_t)p.row_tiles * (p.merge_kernel ? p.splits : p.n_clusters) * 128;
         tc::TcLaunch L;
         memset(&L, 0, sizeof(L));
         tc::TcArgs& a = L.args;
@@ -527,6 +569,8 @@ static fr_status decode_attn_impl(const uint16_t* q16, const float* q, int64_t q
         a.tiles_per_split = p.tiles_per_split;
         a.n_clusters = p.n_clusters;
         a.C = p.C;
+        a.merge_kernel = p.merge_kernel;
+        a.splits = p.splits;
         a.kq_log2 = kq_scale * kLog2e;
         a.wait_limit_ns = tc::kWaitLimitNs;
         a.probe_iters = (uint32_t)o.wait_probe_iters;
@@ -538,7 +582,9 @@ static fr_status decode_attn_impl(const uint16_t* q16, const float* q, int64_t q
         L.m_rs = m_rs;
         L.row_tiles = p.row_tiles;
         L.splits = p.splits;
-        return tc::launch_tc(L, hd, stream);
+        const fr_status st = tc::launch_tc(L, hd, stream);
+        if (st != FR_OK || !p.merge_kernel) return st;
+        return tc::launch_merge(a.part_o, a.part_ml, out, M, p.splits, hd, stream);
     }
 
     const Plan p = make_plan(M, n_kv, sms, o.force_splits);
@@ -580,8 +626,19 @@ using namespace fr;
 extern "C" size_t fr_decode_attn_workspace_size(int n_tok, int n_head, int hd, int n_kv) {
     if (n_tok < 1 || n_tok > kMaxTok || n_head < 1 || (int64_t)n_tok * n_head > kMaxRows) return 0;
     if ((hd != 64 && hd != 128 && hd != 256) || n_kv < 1 || n_kv > (1 << 26)) return 0;
+    const int M = n_tok * n_head;
+    // room for every plan, the merge-kernel one included
+    const size_t base = workspace_bytes_for(M, hd, n_kv);
+    const size_t merge = tc_merge_workspace_bytes(M, hd);
+    return merge > base ? merge : base;
+}
+
+namespace fr {
+size_t decode_attn_min_workspace_bytes(int n_tok, int n_head, int hd, int n_kv) {
+    if (fr_decode_attn_workspace_size(n_tok, n_head, hd, n_kv) == 0) return 0;
     return workspace_bytes_for(n_tok * n_head, hd, n_kv);
 }
+}  // namespace fr
 
 extern "C" fr_status fr_workspace_init(void* ws, size_t ws_bytes, cudaStream_t stream) {
     if (!ws || ws_bytes < kWsHeader) return FR_ERR_INVALID_ARG;

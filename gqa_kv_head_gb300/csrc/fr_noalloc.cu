@@ -15,6 +15,7 @@
 
 #include <cuda_runtime.h>
 
+#include "fr_attn.h"
 #include "fr_kernels.h"
 
 namespace {
@@ -53,7 +54,7 @@ extern "C" fr_status fr_decode_attn_noalloc(const uint16_t* q16, const float* q,
                                             int64_t mask_row_stride, int n_tok, int n_head, int hd, int n_kv,
                                             float kq_scale, float* out, cudaStream_t stream) {
     if (n_tok < 1 || n_head < 1 || n_kv < 1) return FR_ERR_INVALID_ARG;
-    const size_t need = fr_decode_attn_workspace_size(n_tok, n_head, hd, n_kv);
+    const size_t need = fr::decode_attn_min_workspace_bytes(n_tok, n_head, hd, n_kv);
     if (need == 0) return FR_ERR_UNSUPPORTED;
     if (need > kScratchBytes) return FR_ERR_WORKSPACE;       // beyond the fixed scratch
     int dev = 0;

@@ -97,7 +97,7 @@ def _row_stride(t, name):
 
 def decode_attn(k, v, n_tok, n_head, *, q16=None, q=None, pos=None, rope=None, q_scale=None,
                 mask=None, kq_scale=1.0, out=None, workspace=None, splits=None, cluster=None,
-                engine=None, wait_probe_iters=0, stream=None):
+                engine=None, wait_probe_iters=0, merge_mode=None, stream=None):
     """fr_decode_attn (fused qkv_post when q16 is None). Returns out
     [n_tok, n_head, hd] f32. splits / cluster / engine / wait_probe_iters go
     through the fr_decode_attn_ex test hook."""
@@ -124,11 +124,12 @@ def decode_attn(k, v, n_tok, n_head, *, q16=None, q=None, pos=None, rope=None, q
             float(q_scale or 0.0), _ptr(k), _row_stride(k, "k"), _ptr(v), _row_stride(v, "v"),
             _ptr(mask), 0 if mask is None else _row_stride(mask, "mask"), n_tok, n_head, hd, n_kv,
             float(kq_scale), _ptr(out), _ptr(workspace), workspace.numel()]
-    if splits is None and cluster is None and engine is None and not wait_probe_iters:
+    if splits is None and cluster is None and engine is None and not wait_probe_iters and not merge_mode:
         st = lib.fr_decode_attn(*args, _stream(stream))
         _abi.check(st, "fr_decode_attn")
     else:
-        opts = FrAttnOpts(int(engine or 0), int(splits or 0), int(cluster or 0), int(wait_probe_iters))
+        opts = FrAttnOpts(int(engine or 0), int(splits or 0), int(cluster or 0), int(wait_probe_iters),
+                          int(merge_mode or 0))
         st = lib.fr_decode_attn_ex(*args, ctypes.byref(opts), _stream(stream))
         _abi.check(st, "fr_decode_attn_ex")
     return out

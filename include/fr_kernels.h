@@ -107,9 +107,10 @@ fr_status fr_qkv_post(const float* q, int64_t q_tok_stride, const int32_t* pos,
                       uint16_t* q16_out, float* q32_out, cudaStream_t stream);
 
 /*
- * Workspace bytes fr_decode_attn needs for this shape (0 for unsupported
- * shapes). The workspace holds the split-KV partial states, self-resetting
- * arrival tickets and a device status word. Zero it once after allocating it
+ * Workspace bytes for this shape that admit every plan of fr_decode_attn,
+ * the separate merge kernel's included (0 for unsupported shapes). The
+ * workspace holds the split-KV partial states, self-resetting arrival tickets
+ * and a device status word. Zero it once after allocating it
  * (fr_workspace_init); every call leaves the tickets at zero again.
  */
 size_t fr_decode_attn_workspace_size(int n_tok, int n_head, int hd, int n_kv);
@@ -173,6 +174,9 @@ typedef struct fr_attn_opts {
     int wait_probe_iters;  /* > 0: every CTA also polls, this many times, a barrier that is
                               never signalled; fr_workspace_check then reports
                               FR_ERR_DEVICE_TIMEOUT (exercises the timeout path) */
+    int merge_mode;        /* 0 = library's choice; 1 = merge the split states inside the
+                              attention launch (clusters + arrival tickets); 2 = a separate
+                              merge kernel (needs the full workspace size) */
 } fr_attn_opts;
 
 fr_status fr_decode_attn_ex(const uint16_t* q16,
@@ -193,9 +197,10 @@ fr_status fr_decode_attn_ex(const uint16_t* q16,
  *
  * Same arguments and result as fr_decode_attn, minus the workspace. The split
  * state lives in a 9 MiB scratch array inside the library, present on every GPU
- * that loads the library until the process exits. Shapes whose
- * fr_decode_attn_workspace_size() exceeds 9 MiB (in practice hd = 256 with
- * n_tok*n_head > 256) return FR_ERR_WORKSPACE. No device memory is allocated.
+ * that loads the library until the process exits. Within it the library picks
+ * only plans that fit; shapes whose smallest plan (split states merged inside
+ * the attention launch) needs more than 9 MiB, in practice hd = 256 with
+ * n_tok*n_head > 256, return FR_ERR_WORKSPACE. No device memory is allocated.
  * The first call on each device looks up the array's device address
  * (cudaGetSymbolAddress); make that first call before any stream capture. Each
  * call clears the array's status word and arrival tickets on `stream` before

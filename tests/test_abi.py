@@ -88,8 +88,8 @@ def test_decode_attn_validation(lib):
     assert _attn(lib, q16=None) == 1
     from gqa_kv_head_gb300._abi import FrAttnOpts
     ws_ok = lib.fr_decode_attn_workspace_size(4, 8, 128, 64)
-    for bad in (FrAttnOpts(7, 0, 0, 0), FrAttnOpts(0, -1, 0, 0), FrAttnOpts(0, 0, 3, 0),
-                FrAttnOpts(0, 0, 16, 0), FrAttnOpts(0, 0, 0, -5)):
+    for bad in (FrAttnOpts(7, 0, 0, 0, 0), FrAttnOpts(0, -1, 0, 0, 0), FrAttnOpts(0, 0, 3, 0, 0),
+                FrAttnOpts(0, 0, 16, 0, 0), FrAttnOpts(0, 0, 0, -5, 0), FrAttnOpts(0, 0, 0, 0, 3)):
         assert lib.fr_decode_attn_ex(FAKE, None, 0, None, None, 0.0, FAKE, 128, FAKE, 128, None, 0,
                                      4, 8, 128, 64, 1.0, FAKE, FAKE, ws_ok, ctypes.byref(bad), None) == 1
 

@@ -243,3 +243,26 @@ def test_unsupported_returns_status():
     with pytest.raises(fr.FrError):
         fr.decode_attn(d["k"], d["v"], 17, 1, q16=torch.zeros((17, 64), dtype=torch.float16,
                                                                 device="cuda"))
+
+
+@pytest.mark.parametrize("name", ["tiny", "pi05", "c3", "long_decode"])
+@pytest.mark.parametrize("splits", [None, 1, 3])
+def test_merge_kernel_mode(name, splits):
+    """Split states merged by the separate merge kernel (every SM one split)."""
+    w = named_config(name)
+    d = to_device(w)
+    o = _out_rows(run_fused(w, d, merge_mode=2, splits=splits))
+    assert_close(o, oracle_out(w), f"{name} merge kernel splits={splits}")
+
+
+def test_merge_kernel_mode_ragged_and_repeatable():
+    w = Workload("ragged-merge", n_head=5, n_tok=7, hd=64, n_kv=4097,
+                 rope=RopeParams(n_dims=64, freq_base=10000.0),
+                 positions=tuple(range(4096, 4103)), mask_kind="random5", seed=9)
+    d = to_device(w, k_pad=16, mask_pad=8, q_extra_heads=2)
+    ws = fr.make_workspace(w.n_tok, w.n_head, w.hd, w.n_kv)
+    a = run_fused(w, d, merge_mode=2, workspace=ws).clone()
+    b = run_fused(w, d, merge_mode=2, workspace=ws)
+    torch.cuda.synchronize()
+    assert torch.equal(a, b)
+    assert_close(_out_rows(a), oracle_out(w), "ragged merge kernel")
