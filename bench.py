@@ -350,6 +350,8 @@ def run_ours(args, rank, world, local_rank):
                "sample": f"{n_cpu} full oracle calls (fp64 numpy, 1 BLAS thread) on the "
                          f"{w.name} workload, ~{args.cpu_seconds:.0f} s"}
 
+    plan = fr.decode_attn_plan(w.n_tok, w.n_head, w.hd, w.n_kv, workspace_bytes=ws.numel())
+    attn_kernels = "attn_tc_kernel + attn_merge_kernel" if plan["merge_kernel"] else "attn_tc_kernel"
     peak, peak_kind = load_peaks()
     attn_bytes = attention_bytes(w)
     achieved = attn_bytes / (attn_us * 1e-6) / 1e9
@@ -359,7 +361,8 @@ def run_ours(args, rank, world, local_rank):
         "scaling": "weak", "vs_baseline": None, "dtype": "f16", "data": "synthetic",
         "config": config_dict(w),
         "timing": {"launch": f"CUDA graph of {G} back-to-back calls, replayed; each call = "
-                             "qkv_post kernel + attention kernel (programmatic dependent launch)",
+                             f"qkv_post kernel + {attn_kernels} (programmatic dependent launches)",
+                   "plan": plan,
                    "l2": f"inputs rotated over {n_rep} replicas ({n_rep * per_rep / 2**20:.0f} MiB > 2x L2)",
                    "parallelism": "replicas only" if world > 1 else "1 GPU"},
         "kv_gbs": kv_real_bytes / (us_per_call * 1e-6) / 1e9,
@@ -367,12 +370,12 @@ def run_ours(args, rank, world, local_rank):
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": ncu_traffic(args.config),
                      "peak_kind": f"{peak_kind} hbm_gbs (burst copy)",
-                     "kernel": "attn_tc_kernel (decode attention on f16 Q rows)",
+                     "kernel": f"{attn_kernels} (decode attention on f16 Q rows, one call)",
                      "kernel_us_per_launch": attn_us,
                      "algorithmic_bytes_per_launch": attn_bytes},
         "e2e": {"value": e2e_us, "unit": "us/call", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
-        "gpu_launches": 2 * args.steps,      # qkv_post + attention per call
+        "gpu_launches": plan["launches"] * args.steps,
         "clocks": clk,
     }
     if cpu is not None:

@@ -32,6 +32,11 @@ class FrAttnOpts(ctypes.Structure):
                 ("merge_mode", ctypes.c_int)]
 
 
+class FrAttnPlan(ctypes.Structure):
+    _fields_ = [("engine", ctypes.c_int), ("row_tiles", ctypes.c_int), ("splits", ctypes.c_int),
+                ("cluster", ctypes.c_int), ("merge_kernel", ctypes.c_int), ("launches", ctypes.c_int)]
+
+
 _P = ctypes.c_void_p
 _I = ctypes.c_int
 _I64 = ctypes.c_int64
@@ -52,6 +57,8 @@ SIGNATURES = {
     "fr_decode_attn": (_I, _ATTN_ARGS + [_P]),
     "fr_decode_attn_ex": (_I, _ATTN_ARGS + [ctypes.POINTER(FrAttnOpts), _P]),
     "fr_decode_attn_noalloc": (_I, _ATTN_ARGS[:18] + [_P]),
+    "fr_decode_attn_plan": (_I, [_I, _I, _I, _I, _I, _SZ, ctypes.POINTER(FrAttnOpts),
+                                 ctypes.POINTER(FrAttnPlan)]),
 }
 
 _lib = None

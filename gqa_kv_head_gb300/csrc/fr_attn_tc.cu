@@ -94,6 +94,9 @@ struct Cfg {
     static constexpr int RECV_BYTES = kRows * RS * 4;
     static constexpr int TB_BYTES = 8 * 32 * 36 * 4;
     static constexpr int TB_OFF = HD == 256 ? 0 : RECV_OFF + RECV_BYTES;
+    // merge-kernel mode: O rows leave as HD/32 TMA boxes of [128][32] fp32 in the stage area
+    static constexpr int OBOX = kRows * 128;
+    static_assert((HD / 32) * OBOX <= STAGES * STAGE_BYTES, "O boxes inside the stage area");
     static constexpr int BAR_OFF = DATA + AUX;
     // mbarrier slots (8 bytes each), laid out from STAGES
     static constexpr int B_FULL = 0, B_EMPTY = STAGES, B_SFULL = 2 * STAGES, B_PFULL = 2 * STAGES + 2,
@@ -116,6 +119,7 @@ struct Cfg {
 
 struct Maps {
     CUtensorMap k, v, mask, q16;
+    CUtensorMap po;           // merge-kernel mode: split O rows [row_tiles * splits * 128][HD] fp32
 };
 
 __device__ __forceinline__ void record_timeout(unsigned* status, unsigned bit) {
@@ -126,6 +130,10 @@ __device__ __forceinline__ void record_timeout(unsigned* status, unsigned bit) {
 // barriers 1..4, 64 threads each).
 __device__ __forceinline__ void quad_bar_sync(int q) {
     asm volatile("bar.sync %0, 64;" :: "r"(q + 1) : "memory");
+}
+// Barrier over all softmax warps (named barrier 5).
+__device__ __forceinline__ void softmax_bar_sync() {
+    asm volatile("bar.sync 5, %0;" :: "n"(kSmaxThreads) : "memory");
 }
 
 template <int HD>
@@ -420,39 +428,43 @@ attn_tc_kernel(const __grid_constant__ TcArgs a, const __grid_constant__ Maps mp
     cluster_sync();                     // #3: every CTA is done with its data region
 
     if (a.merge_kernel) {
-        // ---- merge-kernel mode: this split's (m, l, O) rows go to the workspace
-        // (coalesced through the transposition buffer); attn_merge_kernel merges them
-        if (warp < kSmaxWarps && quad_active) {
-            tc_fence_after();
-            float* tb_w = sTB + warp * (32 * 36);
-            const int srow = lane >> 3, scol = (lane & 7) * 4;
-            float* base = a.part_o + ((int64_t)(rt * a.splits + split) * kRows) * HD + half * OH;
+        // ---- merge-kernel mode: this split's (m, l, O) rows go to the workspace;
+        // attn_merge_kernel merges them. O leaves TMEM into the stage area (free
+        // now) as HD/32 boxes of [128 rows][32 fp32] in the 128-byte swizzle, and
+        // goes out as TMA tensor stores.
+        if (warp < kSmaxWarps) {
+            unsigned char* sOut = sStage;
+            if (quad_active) {
+                tc_fence_after();
 #pragma unroll 1
-            for (int c = 0; c < OH; c += 32) {
-                uint32_t o[32];
-                if (n_my > 0) {
-                    tmem_ld_x32(tbase + lane_base + C::TM_O + half * OH + c, o);
-                    tmem_wait_ld();
-                } else {
+                for (int c = 0; c < OH; c += 32) {
+                    uint32_t o[32];
+                    if (n_my > 0) {
+                        tmem_ld_x32(tbase + lane_base + C::TM_O + half * OH + c, o);
+                        tmem_wait_ld();
+                    } else {
 #pragma unroll
-                    for (int u = 0; u < 32; ++u) o[u] = 0u;
+                        for (int u = 0; u < 32; ++u) o[u] = 0u;
+                    }
+                    unsigned char* rowp = sOut + ((half * OH + c) >> 5) * C::OBOX + r * 128;
+#pragma unroll
+                    for (int j = 0; j < 8; ++j)
+                        *reinterpret_cast<uint4*>(rowp + ((j ^ (r & 7)) << 4)) =
+                            make_uint4(o[4 * j], o[4 * j + 1], o[4 * j + 2], o[4 * j + 3]);
                 }
-#pragma unroll
-                for (int u = 0; u < 32; u += 4)
-                    *reinterpret_cast<uint4*>(tb_w + lane * 36 + u) = make_uint4(o[u], o[u + 1], o[u + 2], o[u + 3]);
-                __syncwarp();
-#pragma unroll
-                for (int st = 0; st < 8; ++st) {
-                    const int rr = qd * 32 + st * 4 + srow;
-                    if (rr < rows_real)
-                        *reinterpret_cast<uint4*>(base + (int64_t)rr * HD + c + scol) =
-                            *reinterpret_cast<const uint4*>(tb_w + (st * 4 + srow) * 36 + scol);
-                }
-                __syncwarp();
+                if (half == 0 && r < rows_real)
+                    a.part_ml[(int64_t)(rt * a.splits + split) * kRows + r] =
+                        n_my > 0 ? make_float2(m_ref, l_part) : make_float2(-INFINITY, 0.f);
             }
-            if (half == 0 && r < rows_real)
-                a.part_ml[(int64_t)(rt * a.splits + split) * kRows + r] =
-                    n_my > 0 ? make_float2(m_ref, l_part) : make_float2(-INFINITY, 0.f);
+            fence_proxy_async_cta();        // the boxes are read by the TMA engine
+            softmax_bar_sync();
+            if (warp == 0 && lane == 0) {
+                const int y = (rt * a.splits + split) * kRows;
+#pragma unroll 1
+                for (int bx = 0; bx < HD / 32; ++bx) tma_store_2d(&mp.po, bx * 32, y, smem_addr(sOut + bx * C::OBOX));
+                bulk_commit();
+                bulk_wait_all();            // performed before the grid completes
+            }
         }
     } else {
     // ---- push (m, l, O) rows to the CTA that owns them in this cluster ------
@@ -629,9 +641,12 @@ attn_tc_kernel(const __grid_constant__ TcArgs a, const __grid_constant__ Maps mp
 }
 
 // Merge of the split states written in merge-kernel mode. One CTA per (row,
-// 128-column chunk): the split weights 2^(m_s - max m) and the row sum first,
-// then 8 warps each add a fixed subset of the splits (in order) and the warps'
-// sums are added in order: the result does not depend on timing.
+// 128-column chunk), 8 warps; warp w takes splits w, w+8, w+16, ... Every load
+// of a warp (its (m, l) pairs, one per lane, and its O chunks) is issued before
+// any is used. Each warp weighs its splits by 2^(m_s - m_w) against its own
+// maximum m_w; the 8 warp sums are then combined in warp order against the
+// row maximum. The order of every sum is fixed: the result does not depend on
+// timing.
 template <int HD>
 __global__ void __launch_bounds__(256)
 attn_merge_kernel(const float* __restrict__ part_o, const float2* __restrict__ part_ml, float* __restrict__ out,
@@ -639,66 +654,60 @@ attn_merge_kernel(const float* __restrict__ part_o, const float2* __restrict__ p
     constexpr int CWM = HD < 128 ? HD : 128;
     constexpr int NCH = HD / CWM;
     constexpr int LANES = CWM / 4;
-    __shared__ float s_m[kMaxMergeSplits], s_w[kMaxMergeSplits], s_l[kMaxMergeSplits];
-    __shared__ float s_red[8][CWM];
-    __shared__ float s_max[8], s_sum[8];
+    constexpr int PER_WARP = (kMaxMergeSplits + 7) / 8;
+    static_assert(PER_WARP <= 32, "one (m, l) pair per lane");
+    __shared__ float s_acc[8][CWM];
+    __shared__ float s_m[8], s_l[8];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int row = blockIdx.x / NCH, chunk = blockIdx.x - row * NCH;
     const int rt = row >> 7, rr = row & 127;
     asm volatile("griddepcontrol.wait;" ::: "memory");     // the attention grid is complete
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    const int n_w = splits > warp ? (splits - warp + 7) / 8 : 0;   // splits of this warp
     const float2* ml = part_ml + (int64_t)rt * splits * kRows + rr;
-    float mx = -INFINITY;
-    for (int s2 = tid; s2 < splits; s2 += 256) {
-        const float2 v = __ldcg(ml + (int64_t)s2 * kRows);
-        s_m[s2] = v.x;
-        s_l[s2] = v.y;
-        mx = fmaxf(mx, v.x);
-    }
-    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-    if (lane == 0) s_max[warp] = mx;
-    __syncthreads();
-    mx = s_max[0];
-    for (int w = 1; w < 8; ++w) mx = fmaxf(mx, s_max[w]);
-    const float ref = mx == -INFINITY ? 0.f : mx;
-    float lsum = 0.f;
-    for (int s2 = tid; s2 < splits; s2 += 256) {
-        const float w = s_m[s2] == -INFINITY ? 0.f : ex2(s_m[s2] - ref);
-        s_w[s2] = w;
-        lsum = fmaf(w, s_l[s2], lsum);
-    }
-    for (int o = 16; o > 0; o >>= 1) lsum += __shfl_xor_sync(0xffffffffu, lsum, o);
-    if (lane == 0) s_sum[warp] = lsum;
-    __syncthreads();
-    float L = 0.f;
-    for (int w = 0; w < 8; ++w) L += s_sum[w];
+    const float2 my_ml = lane < n_w ? __ldcg(ml + (int64_t)(warp + 8 * lane) * kRows) : make_float2(-INFINITY, 0.f);
+    float4 v[PER_WARP];
+    const float* base = part_o + ((int64_t)rt * splits * kRows + rr) * HD + chunk * CWM + (lane % LANES) * 4;
+    const int64_t sstride = (int64_t)kRows * HD;
+#pragma unroll
+    for (int u = 0; u < PER_WARP; ++u)
+        v[u] = (u < n_w && lane < LANES) ? __ldcg(reinterpret_cast<const float4*>(base + (warp + 8 * u) * sstride))
+                                         : make_float4(0.f, 0.f, 0.f, 0.f);
+    float mw = my_ml.x;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mw = fmaxf(mw, __shfl_xor_sync(0xffffffffu, mw, o));
+    const float ref = mw == -INFINITY ? 0.f : mw;
+    const float my_w = my_ml.x == -INFINITY ? 0.f : ex2(my_ml.x - ref);
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (lane < LANES) {
-        const float* base = part_o + ((int64_t)rt * splits * kRows + rr) * HD + chunk * CWM + lane * 4;
-        const int64_t sstride = (int64_t)kRows * HD;
-        for (int s0 = warp; s0 < splits; s0 += 8 * 4) {
-            float4 v[4];
+    float lw = 0.f;
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {               // four independent loads in flight
-                const int s2 = s0 + 8 * u;
-                v[u] = s2 < splits ? __ldcg(reinterpret_cast<const float4*>(base + s2 * sstride))
-                                   : make_float4(0.f, 0.f, 0.f, 0.f);
-            }
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const int s2 = s0 + 8 * u;
-                const float w = s2 < splits ? s_w[s2] : 0.f;
-                acc.x = fmaf(w, v[u].x, acc.x);
-                acc.y = fmaf(w, v[u].y, acc.y);
-                acc.z = fmaf(w, v[u].z, acc.z);
-                acc.w = fmaf(w, v[u].w, acc.w);
-            }
-        }
-        *reinterpret_cast<float4*>(&s_red[warp][lane * 4]) = acc;
+    for (int u = 0; u < PER_WARP; ++u) {
+        const float w = __shfl_sync(0xffffffffu, my_w, u);
+        const float l = __shfl_sync(0xffffffffu, my_ml.y, u);
+        lw = fmaf(w, l, lw);
+        acc.x = fmaf(w, v[u].x, acc.x);
+        acc.y = fmaf(w, v[u].y, acc.y);
+        acc.z = fmaf(w, v[u].z, acc.z);
+        acc.w = fmaf(w, v[u].w, acc.w);
+    }
+    if (lane < LANES) *reinterpret_cast<float4*>(&s_acc[warp][lane * 4]) = acc;
+    if (lane == 0) {
+        s_m[warp] = mw;
+        s_l[warp] = lw;
     }
     __syncthreads();
     if (tid < CWM && row < M) {
-        float sum = 0.f;
-        for (int w = 0; w < 8; ++w) sum += s_red[w][tid];
+        float mx = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < 8; ++w) mx = fmaxf(mx, s_m[w]);
+        const float mref = mx == -INFINITY ? 0.f : mx;
+        float sum = 0.f, L = 0.f;
+#pragma unroll
+        for (int w = 0; w < 8; ++w) {
+            const float sc = s_m[w] == -INFINITY ? 0.f : ex2(s_m[w] - mref);
+            sum = fmaf(sc, s_acc[w][tid], sum);
+            L = fmaf(sc, s_l[w], L);
+        }
         out[(int64_t)row * HD + chunk * CWM + tid] = L > 0.f ? sum / L : 0.f;
     }
 }
@@ -754,6 +763,20 @@ static bool encode_2d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 2-D fp32 tensor [rows][inner], contiguous rows; boxes of 32 columns (128 B) x
+// box_rows in the 128-byte swizzle (the layout the merge-kernel epilogue writes).
+static bool encode_2d_f32(CUtensorMap* m, void* base, uint64_t inner, uint64_t rows, uint32_t box_rows) {
+    auto enc = get_encoder();
+    if (!enc) return false;
+    cuuint64_t dims[2] = {inner, rows};
+    cuuint64_t strides[1] = {inner * 4};
+    cuuint32_t box[2] = {32, box_rows};
+    cuuint32_t es[2] = {1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, base, dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+               CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 template <int HD>
 static cudaError_t ensure_attr(int dev) {
     static unsigned long long done = 0ull;
@@ -778,6 +801,9 @@ static fr_status launch(const TcLaunch& L, cudaStream_t stream) {
     if (!encode_2d(&mp.v, L.v, HD, a.n_kv, L.v_rs, 64, BN)) return FR_ERR_CUDA;
     if (a.has_mask && !encode_2d(&mp.mask, L.mask, a.n_kv, a.n_tok, L.m_rs, 64, a.n_tok)) return FR_ERR_CUDA;
     if (!a.q16 || !encode_2d(&mp.q16, a.q16, HD, a.M, HD, 64, kRows / a.C)) return FR_ERR_CUDA;
+    if (a.merge_kernel &&
+        !encode_2d_f32(&mp.po, a.part_o, HD, (uint64_t)L.row_tiles * a.splits * kRows, kRows))
+        return FR_ERR_CUDA;
 
     cudaLaunchConfig_t cfg;
     memset(&cfg, 0, sizeof(cfg));

@@ -393,10 +393,13 @@ static size_t tc_workspace_bytes(int M, int hd) {
 }
 
 // merge-kernel mode: [header][f16 Q rows][split O [row_tiles][splits][128][hd]][split (m, l)]
+static size_t tc_merge_fixed_bytes(int M, int hd) { return kWsHeader + tc_q16_bytes(M, hd); }
+static size_t tc_merge_split_bytes(int M, int hd) {      // per split of every row tile
+    return (size_t)((M + 127) / 128) * 128 * (hd * sizeof(float) + sizeof(float2));
+}
+static int tc_merge_max_splits(int M) { return tc::kMaxMergeSplits / ((M + 127) / 128); }
 static size_t tc_merge_workspace_bytes(int M, int hd) {
-    const size_t row_tiles = (size_t)(M + 127) / 128;
-    const size_t slots = row_tiles * ((tc::kMaxMergeSplits + row_tiles - 1) / row_tiles) * 128;
-    return kWsHeader + tc_q16_bytes(M, hd) + slots * hd * sizeof(float) + slots * sizeof(float2);
+    return tc_merge_fixed_bytes(M, hd) + (size_t)tc_merge_max_splits(M) * tc_merge_split_bytes(M, hd);
 }
 
 // Smallest workspace any plan of this shape accepts (in-kernel merge).
@@ -446,26 +449,34 @@ static TcPlan make_tc_plan(int M, int hd, int n_kv, int num_sms, int force_split
     return p;
 }
 
-// Many splits make the in-kernel merge's serial tail dominate; then every SM
-// takes one split without clusters and a separate merge kernel reduces the
-// states with the whole GPU. Chosen when the cluster plan needs more than 4
-// clusters per row tile and the workspace holds the split states.
+// Beyond two splits the in-launch merge (DSMEM pushes at a few tens of GB/s
+// per SM, then the last CTA per slice reading every cluster's slice) costs
+// more than a second launch; then every SM takes one split without clusters
+// and a separate merge kernel reduces the states with the whole GPU. The
+// split count is cut to what the workspace holds; in the automatic choice a
+// workspace too small for the full count keeps the in-launch plan.
 static TcPlan choose_tc_plan(int M, int hd, int n_kv, int num_sms, const fr_attn_opts& o, size_t ws_bytes,
                              bool* ok) {
     TcPlan p = make_tc_plan(M, hd, n_kv, num_sms, o.force_splits, o.force_cluster);
     *ok = true;
-    const bool fits = ws_bytes >= tc_merge_workspace_bytes(M, hd);
-    bool use = false;
-    if (o.merge_mode == 2) {
-        use = true;
-        if (!fits) *ok = false;
-    } else if (o.merge_mode == 0 && o.force_cluster == 0) {
-        use = p.n_clusters > 4 && fits;
-    }
+    bool use;
+    if (o.merge_mode == 2) use = true;
+    else if (o.merge_mode == 1 || o.force_cluster != 0) use = false;
+    else use = p.splits > 2;
     if (!use) return p;
-    const int cap = tc::kMaxMergeSplits / p.row_tiles;
+    const int cap = tc_merge_max_splits(M);
     int S = o.force_splits > 0 ? o.force_splits : max(1, num_sms / p.row_tiles);
-    S = max(1, min(S, min(cap, o.force_splits > 0 ? p.n_tiles : (p.n_tiles + 1) / 2)));
+    S = max(1, min(S, min(cap, p.n_tiles)));
+    const size_t fixed = tc_merge_fixed_bytes(M, hd);
+    const int fit = ws_bytes > fixed ? (int)min((size_t)cap, (ws_bytes - fixed) / tc_merge_split_bytes(M, hd)) : 0;
+    if (fit < S) {
+        if (o.merge_mode != 2) return p;
+        if (o.force_splits > 0 || fit < 1) {
+            *ok = false;
+            return p;
+        }
+        S = fit;
+    }
     p.tiles_per_split = (p.n_tiles + S - 1) / S;
     p.splits = (p.n_tiles + p.tiles_per_split - 1) / p.tiles_per_split;
     p.C = 1;
@@ -631,6 +642,44 @@ extern "C" size_t fr_decode_attn_workspace_size(int n_tok, int n_head, int hd, i
     const size_t base = workspace_bytes_for(M, hd, n_kv);
     const size_t merge = tc_merge_workspace_bytes(M, hd);
     return merge > base ? merge : base;
+}
+
+extern "C" fr_status fr_decode_attn_plan(int n_tok, int n_head, int hd, int n_kv, int fused_qkv_post,
+                                         size_t workspace_bytes, const fr_attn_opts* opts, fr_attn_plan* plan) {
+    if (!plan) return FR_ERR_INVALID_ARG;
+    if (fr_decode_attn_workspace_size(n_tok, n_head, hd, n_kv) == 0) return FR_ERR_UNSUPPORTED;
+    fr_attn_opts o;
+    memset(&o, 0, sizeof(o));
+    if (opts) o = *opts;
+    if (o.engine < 0 || o.engine > 1 || o.force_splits < 0 || o.merge_mode < 0 || o.merge_mode > 2)
+        return FR_ERR_INVALID_ARG;
+    if (o.force_cluster != 0 && o.force_cluster != 1 && o.force_cluster != 2 && o.force_cluster != 4 &&
+        o.force_cluster != 8)
+        return FR_ERR_INVALID_ARG;
+    const int M = n_tok * n_head;
+    if (workspace_bytes < workspace_bytes_for(M, hd, n_kv)) return FR_ERR_WORKSPACE;
+    int dev = 0, sms = 152;
+    if (cudaGetDevice(&dev) != cudaSuccess) return FR_ERR_CUDA;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return FR_ERR_CUDA;
+    memset(plan, 0, sizeof(*plan));
+    plan->engine = o.engine;
+    if (o.engine == 0) {
+        bool ok = true;
+        const TcPlan p = choose_tc_plan(M, hd, n_kv, sms, o, workspace_bytes, &ok);
+        if (!ok) return FR_ERR_WORKSPACE;
+        plan->row_tiles = p.row_tiles;
+        plan->splits = p.splits;
+        plan->cluster = p.C;
+        plan->merge_kernel = p.merge_kernel;
+    } else {
+        const Plan p = make_plan(M, n_kv, sms, o.force_splits);
+        plan->row_tiles = p.n_rb;
+        plan->splits = p.n_splits;
+        plan->cluster = 1;
+        plan->merge_kernel = 0;
+    }
+    plan->launches = (fused_qkv_post && o.engine == 0 ? 1 : 0) + 1 + plan->merge_kernel;
+    return FR_OK;
 }
 
 namespace fr {

@@ -8,6 +8,7 @@
 // FlashRT-llama.cpp development guide, "Invariants and pitfalls": RoPE mirrors
 // ggml's rope_neox with the YaRN corrections; non-NEOX modes are not offered.
 #include <math.h>
+#include <string.h>
 
 #include "fr_common.cuh"
 
@@ -73,8 +74,11 @@ __global__ void __launch_bounds__(256)
 qkv_post_kernel(const float* __restrict__ q, int64_t q_tok_stride, const int32_t* __restrict__ pos,
                 int n_head, int M, __half* __restrict__ q16, float* __restrict__ q32,
                 const __grid_constant__ RopeTable tb) {
-    // a dependent attention launch may start its set-up and K/V loads now; it
-    // waits for this grid's completion before it reads the rows
+    // Launched with programmatic stream serialization: wait until the grids
+    // before this one on the stream are complete and their writes visible. A
+    // dependent attention launch may then start its set-up and K/V loads; it
+    // waits for this grid's completion before it reads the rows.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int r = blockIdx.x * blockDim.y + threadIdx.y;
     if (r >= M) return;
@@ -102,12 +106,25 @@ fr_status launch_qkv_post(const float* q, int64_t q_tok_stride, const int32_t* p
     dim3 block(slots, rows_per_block);
     dim3 grid((M + rows_per_block - 1) / rows_per_block);
     __half* o16 = reinterpret_cast<__half*>(q16_out);
+    // programmatic dependent launch: this grid may be scheduled while the
+    // previous one on the stream finishes (the kernel waits before any access)
+    cudaLaunchConfig_t cfg;
+    memset(&cfg, 0, sizeof(cfg));
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e;
     switch (hd) {
-        case 64: qkv_post_kernel<64><<<grid, block, 0, stream>>>(q, q_tok_stride, pos, n_head, M, o16, q32_out, tb); break;
-        case 128: qkv_post_kernel<128><<<grid, block, 0, stream>>>(q, q_tok_stride, pos, n_head, M, o16, q32_out, tb); break;
-        default: qkv_post_kernel<256><<<grid, block, 0, stream>>>(q, q_tok_stride, pos, n_head, M, o16, q32_out, tb); break;
+        case 64: e = cudaLaunchKernelEx(&cfg, qkv_post_kernel<64>, q, q_tok_stride, pos, n_head, M, o16, q32_out, tb); break;
+        case 128: e = cudaLaunchKernelEx(&cfg, qkv_post_kernel<128>, q, q_tok_stride, pos, n_head, M, o16, q32_out, tb); break;
+        default: e = cudaLaunchKernelEx(&cfg, qkv_post_kernel<256>, q, q_tok_stride, pos, n_head, M, o16, q32_out, tb); break;
     }
-    return cudaGetLastError() == cudaSuccess ? FR_OK : FR_ERR_CUDA;
+    return e == cudaSuccess ? FR_OK : FR_ERR_CUDA;
 }
 
 }  // namespace fr

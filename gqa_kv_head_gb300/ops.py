@@ -135,6 +135,22 @@ def decode_attn(k, v, n_tok, n_head, *, q16=None, q=None, pos=None, rope=None, q
     return out
 
 
+def decode_attn_plan(n_tok, n_head, hd, n_kv, *, fused_qkv_post=True, workspace_bytes=None,
+                     splits=None, cluster=None, engine=None, merge_mode=None):
+    """fr_decode_attn_plan: the launch shape a call with these arguments would
+    use on the current device (nothing is launched). Returns a dict with
+    engine, row_tiles, splits, cluster, merge_kernel, launches."""
+    lib = _abi.load()
+    if workspace_bytes is None:
+        workspace_bytes = workspace_size(n_tok, n_head, hd, n_kv)
+    opts = FrAttnOpts(int(engine or 0), int(splits or 0), int(cluster or 0), 0, int(merge_mode or 0))
+    plan = _abi.FrAttnPlan()
+    st = lib.fr_decode_attn_plan(n_tok, n_head, hd, n_kv, 1 if fused_qkv_post else 0, int(workspace_bytes),
+                                 ctypes.byref(opts), ctypes.byref(plan))
+    _abi.check(st, "fr_decode_attn_plan")
+    return {name: getattr(plan, name) for name, _ in plan._fields_}
+
+
 def decode_attn_noalloc(k, v, n_tok, n_head, *, q16=None, q=None, pos=None, rope=None, q_scale=None,
                         mask=None, kq_scale=1.0, out=None, stream=None):
     """fr_decode_attn_noalloc: the same attention without a workspace, for

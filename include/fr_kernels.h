@@ -176,7 +176,8 @@ typedef struct fr_attn_opts {
                               FR_ERR_DEVICE_TIMEOUT (exercises the timeout path) */
     int merge_mode;        /* 0 = library's choice; 1 = merge the split states inside the
                               attention launch (clusters + arrival tickets); 2 = a separate
-                              merge kernel (needs the full workspace size) */
+                              merge kernel (split count cut to what the workspace holds;
+                              FR_ERR_WORKSPACE if forced splits do not fit) */
 } fr_attn_opts;
 
 fr_status fr_decode_attn_ex(const uint16_t* q16,
@@ -188,6 +189,25 @@ fr_status fr_decode_attn_ex(const uint16_t* q16,
                             int n_tok, int n_head, int hd, int n_kv, float kq_scale,
                             float* out, void* workspace, size_t workspace_bytes,
                             const fr_attn_opts* opts, cudaStream_t stream);
+
+/*
+ * Launch shape fr_decode_attn / fr_decode_attn_ex would use for this shape on
+ * the current device, with a workspace of workspace_bytes and these options
+ * (opts may be NULL); nothing is launched. fused_qkv_post != 0 describes the
+ * call with q16 == NULL. FlashRT PR #185 has no counterpart: the pages' host
+ * adapter sizes its launches internally.
+ */
+typedef struct fr_attn_plan {
+    int engine;            /* 0 tcgen05 kernel, 1 mma.sync kernel */
+    int row_tiles;         /* query-row tiles (128 rows tcgen05, 64 mma.sync) */
+    int splits;            /* KV splits per row tile */
+    int cluster;           /* CTAs per thread-block cluster (1 = none) */
+    int merge_kernel;      /* 1: split states merged by a separate kernel */
+    int launches;          /* kernels one call launches (qkv_post, attention, merge) */
+} fr_attn_plan;
+
+fr_status fr_decode_attn_plan(int n_tok, int n_head, int hd, int n_kv, int fused_qkv_post,
+                              size_t workspace_bytes, const fr_attn_opts* opts, fr_attn_plan* plan);
 
 /*
  * fr_decode_attn_noalloc -- fr_decode_attn without a workspace argument, for

@@ -114,6 +114,29 @@ def test_qkv_post_validation(lib):
     assert call(rp=rope_params(128, ext_factor=1.0, n_ctx_orig=0)) == 1
 
 
+def test_plan_validation(lib):
+    from gqa_kv_head_gb300._abi import FrAttnOpts, FrAttnPlan
+    plan = FrAttnPlan()
+    ws_ok = lib.fr_decode_attn_workspace_size(10, 8, 256, 1024)
+    call = lambda n_tok=10, hd=256, ws=ws_ok, opts=None, out=ctypes.byref(plan): lib.fr_decode_attn_plan(
+        n_tok, 8, hd, 1024, 1, ws, opts, out)
+    assert call(out=None) == 1
+    assert call(hd=96) == 2
+    assert call(n_tok=17) == 2
+    assert call(ws=64) == 3
+    assert call(opts=ctypes.byref(FrAttnOpts(0, 0, 0, 0, 5))) == 1
+    assert call(opts=ctypes.byref(FrAttnOpts(0, 0, 3, 0, 0))) == 1
+
+
+def test_workspace_size_covers_the_merge_kernel_plan(lib):
+    # room for the most splits any plan uses: 160 over the row tiles, each split
+    # 128 rows of hd fp32 plus an (m, l) pair per row
+    ws = lib.fr_decode_attn_workspace_size
+    for n_tok, n_head, hd in ((10, 8, 256), (16, 32, 128), (1, 4, 64)):
+        rt = (n_tok * n_head + 127) // 128
+        assert ws(n_tok, n_head, hd, 1024) >= (160 // rt) * rt * 128 * (hd * 4 + 8)
+
+
 def test_workspace_init_rejects_null(lib):
     assert lib.fr_workspace_init(None, 4096, None) == 1
     assert lib.fr_workspace_check(None, None) == 1

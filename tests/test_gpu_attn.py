@@ -266,3 +266,39 @@ def test_merge_kernel_mode_ragged_and_repeatable():
     torch.cuda.synchronize()
     assert torch.equal(a, b)
     assert_close(_out_rows(a), oracle_out(w), "ragged merge kernel")
+
+
+def test_plan_reports_the_launch_shape():
+    """fr_decode_attn_plan: one or two splits keep the in-launch merge, more
+    splits go to the merge kernel; launches count qkv_post, attention, merge."""
+    tiny = named_config("tiny")
+    p = fr.decode_attn_plan(tiny.n_tok, tiny.n_head, tiny.hd, tiny.n_kv)
+    assert p["engine"] == 0 and p["merge_kernel"] == 0 and p["launches"] == 2 and p["splits"] <= 2
+    w = named_config("pi05")
+    p = fr.decode_attn_plan(w.n_tok, w.n_head, w.hd, w.n_kv)
+    assert p["merge_kernel"] == 1 and p["cluster"] == 1 and p["launches"] == 3
+    assert p["splits"] == 16                        # one 64-key tile per split
+    assert fr.decode_attn_plan(w.n_tok, w.n_head, w.hd, w.n_kv, fused_qkv_post=False)["launches"] == 2
+    p1 = fr.decode_attn_plan(w.n_tok, w.n_head, w.hd, w.n_kv, merge_mode=1)
+    assert p1["merge_kernel"] == 0 and p1["cluster"] > 1 and p1["launches"] == 2
+    # a workspace of the in-launch size only keeps the in-launch plan, or cuts
+    # the split count when the merge kernel is forced
+    lw = named_config("long_decode")
+    small = 9 << 20
+    assert fr.decode_attn_plan(lw.n_tok, lw.n_head, lw.hd, lw.n_kv, workspace_bytes=small)["merge_kernel"] == 0
+    pf = fr.decode_attn_plan(lw.n_tok, lw.n_head, lw.hd, lw.n_kv, workspace_bytes=small, merge_mode=2)
+    assert pf["merge_kernel"] == 1 and pf["splits"] * pf["row_tiles"] * 128 * (lw.hd * 4 + 8) <= small
+    assert fr.decode_attn_plan(w.n_tok, w.n_head, w.hd, w.n_kv, engine=1)["launches"] == 1
+
+
+def test_forced_merge_kernel_with_cut_split_count():
+    """merge_mode 2 with a workspace that holds fewer splits than the default:
+    the split count is cut to fit and the result still matches the oracle."""
+    w = named_config("long_decode")
+    d = to_device(w)
+    nbytes = 9 << 20
+    ws = torch.zeros(nbytes, dtype=torch.uint8, device="cuda")
+    p = fr.decode_attn_plan(w.n_tok, w.n_head, w.hd, w.n_kv, workspace_bytes=nbytes, merge_mode=2)
+    assert p["merge_kernel"] == 1
+    o = _out_rows(run_fused(w, d, merge_mode=2, workspace=ws))
+    assert_close(o, oracle_out(w), "long decode, merge kernel in a 9 MiB workspace")
