@@ -18,7 +18,9 @@
 //              terms, P = P_hi + P_lo (P_lo = f16(p - P_hi)), so the weights
 //              keep ~22 bits and the softmax stays fp32-accurate even where |V|
 //              is large.
-//   warp 8     TMA producer: K, V and mask tiles into a ring of stages; the
+//   warp 8     TMA producer: one thread fills separate rings of K, V and
+//              mask tiles, refilling whichever slot frees first (a K slot is
+//              free again once S_j is computed, so K runs ahead of V); the
 //              first tiles are requested before the Q prologue.
 //   warp 9     MMA issuer: S_j = Q K_j^T (SS form, S double-buffered in TMEM),
 //              O += P_hi,j V_j + P_lo,j V_j (A operand from TMEM, V read
@@ -69,7 +71,12 @@ constexpr uint32_t kTmemCols = 512;
 template <int HD>
 struct Cfg {
     static constexpr int BN = 64;                          // keys per tile
-    static constexpr int STAGES = HD == 256 ? 2 : (HD == 128 ? 5 : 8);
+    // Separate rings for K, V and mask tiles: a K slot frees when S_j is
+    // computed, a V slot when PV_j is, a mask slot when the softmax has read
+    // it, so K tiles run ahead of the V tiles they travel with.
+    static constexpr int KS = HD == 256 ? 2 : (HD == 128 ? 5 : 8);   // K slots
+    static constexpr int VS = KS;                                     // V slots
+    static constexpr int MS = 4;                                      // mask slots
     static constexpr int NB = HD / 64;                     // 128-byte column boxes per row
     static constexpr int Q_BYTES = kRows * HD * 2;
     static constexpr int Q_BOX = kRows * 128;              // one 64-column box of Q
@@ -77,8 +84,9 @@ struct Cfg {
     static constexpr int K_BYTES = BN * HD * 2;
     static constexpr int MASK_BOX = 2048;                  // <= 16 rows x 128 B, 1024-aligned slots
     static constexpr int MASK_BYTES = (BN / 64) * MASK_BOX;
-    static constexpr int STAGE_BYTES = 2 * K_BYTES + MASK_BYTES;
-    static constexpr int BODY = Q_BYTES + STAGES * STAGE_BYTES;
+    static constexpr int K_OFF = 0, V_OFF = KS * K_BYTES, M_OFF = V_OFF + VS * K_BYTES;   // in the stage area
+    static constexpr int STAGE_AREA = M_OFF + MS * MASK_BYTES;
+    static constexpr int BODY = Q_BYTES + STAGE_AREA;
     static constexpr int DATA = BODY;
     static constexpr int AUX = 20480;                      // cos/sin table; then exchange + merge weights
     static constexpr int AUX_MAXX = 0;                     // [2][2][128] f32 half-row maxima
@@ -96,24 +104,26 @@ struct Cfg {
     static constexpr int TB_OFF = HD == 256 ? 0 : RECV_OFF + RECV_BYTES;
     // merge-kernel mode: O rows leave as HD/32 TMA boxes of [128][32] fp32 in the stage area
     static constexpr int OBOX = kRows * 128;
-    static_assert((HD / 32) * OBOX <= STAGES * STAGE_BYTES, "O boxes inside the stage area");
+    static_assert((HD / 32) * OBOX <= STAGE_AREA, "O boxes inside the stage area");
     static constexpr int BAR_OFF = DATA + AUX;
-    // mbarrier slots (8 bytes each), laid out from STAGES
-    static constexpr int B_FULL = 0, B_EMPTY = STAGES, B_SFULL = 2 * STAGES, B_PFULL = 2 * STAGES + 2,
-                         B_ODONE = 2 * STAGES + 4, B_QFULL = 2 * STAGES + 5, B_PROBE = 2 * STAGES + 6,
-                         B_MMADONE = 2 * STAGES + 7, N_BARS = 2 * STAGES + 8;
-    static constexpr int TMEM_SLOT = 32 * 8;               // TMEM base word after 32 barrier slots
-    static_assert(N_BARS <= 32, "barrier slots");
+    // mbarrier slots (8 bytes each), laid out from the ring depths
+    static constexpr int B_KFULL = 0, B_KEMPTY = KS, B_VFULL = 2 * KS, B_VEMPTY = 2 * KS + VS,
+                         B_MFULL = 2 * (KS + VS), B_MEMPTY = 2 * (KS + VS) + MS, B_SFULL = 2 * (KS + VS + MS),
+                         B_PFULL = B_SFULL + 2, B_ODONE = B_SFULL + 4, B_QFULL = B_SFULL + 5,
+                         B_PROBE = B_SFULL + 6, B_MMADONE = B_SFULL + 7, N_BARS = B_SFULL + 8;
+    static constexpr int TMEM_SLOT = 120 * 8;              // TMEM base word after 120 barrier slots
+    static_assert(N_BARS <= 120, "barrier slots");
     static_assert(RECV_OFF + RECV_BYTES <= BODY, "receive area inside the data region");
     static_assert(HD == 256 ? TB_BYTES <= Q_BYTES : TB_OFF + TB_BYTES <= BODY, "transposition buffer");
-    static constexpr int SMEM = BAR_OFF + 512 + 1024;      // barriers + TMEM word, + alignment slack
+    static constexpr int SMEM = BAR_OFF + 1024 + 1024;     // barriers + TMEM word, + alignment slack
     // TMEM columns
     static constexpr int TM_O = 0;
     static constexpr int TM_S = HD;
     static constexpr int TM_P = HD + 2 * BN;               // P_hi, 2 x BN/2 columns
     static constexpr int TM_PL = TM_P + BN;                // P_lo, 2 x BN/2 columns
     static_assert(TM_PL + BN <= (int)kTmemCols, "TMEM budget");
-    static_assert(STAGE_BYTES % 1024 == 0 && Q_BYTES % 1024 == 0, "1024-B alignment of swizzled tiles");
+    static_assert(K_BYTES % 1024 == 0 && MASK_BYTES % 1024 == 0 && Q_BYTES % 1024 == 0,
+                  "1024-B alignment of swizzled tiles");
     static_assert(SMEM <= 232448, "shared memory budget");
 };
 
@@ -179,16 +189,24 @@ attn_tc_kernel(const __grid_constant__ TcArgs a, const __grid_constant__ Maps mp
     };
 
     auto bar = [&](int i) { return smem_addr(&bars[i]); };
-    auto sK = [&](int s) { return sStage + s * C::STAGE_BYTES; };
-    auto sV = [&](int s) { return sStage + s * C::STAGE_BYTES + C::K_BYTES; };
-    auto sMask = [&](int s) { return sStage + s * C::STAGE_BYTES + 2 * C::K_BYTES; };
+    auto sK = [&](int s) { return sStage + C::K_OFF + s * C::K_BYTES; };
+    auto sV = [&](int s) { return sStage + C::V_OFF + s * C::K_BYTES; };
+    auto sMask = [&](int s) { return sStage + C::M_OFF + s * C::MASK_BYTES; };
 
     // ---- set-up ------------------------------------------------------------
     const int my_r0 = (int)rank * R;
     if (tid == 0) {
-        for (int s = 0; s < C::STAGES; ++s) {
-            mbar_init(bar(C::B_FULL + s), 1);
-            mbar_init(bar(C::B_EMPTY + s), 1);
+        for (int s = 0; s < C::KS; ++s) {
+            mbar_init(bar(C::B_KFULL + s), 1);
+            mbar_init(bar(C::B_KEMPTY + s), 1);
+        }
+        for (int s = 0; s < C::VS; ++s) {
+            mbar_init(bar(C::B_VFULL + s), 1);
+            mbar_init(bar(C::B_VEMPTY + s), 1);
+        }
+        for (int s = 0; s < C::MS; ++s) {
+            mbar_init(bar(C::B_MFULL + s), 1);
+            mbar_init(bar(C::B_MEMPTY + s), kSmaxWarps);      // one arrival per softmax warp
         }
         mbar_init(bar(C::B_SFULL + 0), 1);
         mbar_init(bar(C::B_SFULL + 1), 1);
@@ -206,33 +224,48 @@ attn_tc_kernel(const __grid_constant__ TcArgs a, const __grid_constant__ Maps mp
     }
     if (warp == kMmaWarp) tmem_alloc(smem_addr(sTmemBase), kTmemCols);
     tc_fence_before();
-    cluster_sync();                     // #1: barriers of every CTA initialised and armed
+    if (CS > 1) cluster_sync();         // #1: barriers of every CTA initialised and armed
+    else __syncthreads();               //     (one-CTA cluster: a CTA barrier is enough)
     tc_fence_after();
     const uint32_t tbase = *sTmemBase;
     // a dependent merge grid (merge-kernel mode) may be scheduled now; it waits
     // for this grid's completion before reading the split states
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
-    // K/V/mask tiles need no Q: the first ones are requested before the prologue
+    // K/V/mask tiles need no Q: the first ones are requested before the
+    // prologue.
     const uint32_t mask_tx = a.has_mask ? (uint32_t)(BN / 64) * 128u * (uint32_t)a.n_tok : 0u;
-    auto issue_load = [&](int i) {
-        const int st = i % C::STAGES;
-        mbar_expect_tx(bar(C::B_FULL + st), 2u * C::K_BYTES + mask_tx);
-        const int j0 = (t0 + i) * BN;
+    auto load_k = [&](int i) {
+        const int st = i % C::KS;
+        mbar_expect_tx(bar(C::B_KFULL + st), (uint32_t)C::K_BYTES);
 #pragma unroll
-        for (int b = 0; b < C::NB; ++b) {
-            tma_load_2d(smem_addr(sK(st) + b * C::KV_BOX), &mp.k, b * 64, j0, bar(C::B_FULL + st));
-            tma_load_2d(smem_addr(sV(st) + b * C::KV_BOX), &mp.v, b * 64, j0, bar(C::B_FULL + st));
-        }
-        if (a.has_mask) {
-#pragma unroll
-            for (int mb = 0; mb < BN / 64; ++mb)
-                tma_load_2d(smem_addr(sMask(st) + mb * C::MASK_BOX), &mp.mask, j0 + mb * 64, 0, bar(C::B_FULL + st));
-        }
+        for (int b = 0; b < C::NB; ++b)
+            tma_load_2d(smem_addr(sK(st) + b * C::KV_BOX), &mp.k, b * 64, (t0 + i) * BN, bar(C::B_KFULL + st));
     };
-    const int n_pre = min(C::STAGES, n_my);
-    if (warp == kProdWarp && lane == 0)
-        for (int i = 0; i < n_pre; ++i) issue_load(i);
+    auto load_v = [&](int i) {
+        const int st = i % C::VS;
+        mbar_expect_tx(bar(C::B_VFULL + st), (uint32_t)C::K_BYTES);
+#pragma unroll
+        for (int b = 0; b < C::NB; ++b)
+            tma_load_2d(smem_addr(sV(st) + b * C::KV_BOX), &mp.v, b * 64, (t0 + i) * BN, bar(C::B_VFULL + st));
+    };
+    auto load_m = [&](int i) {
+        const int st = i % C::MS;
+        mbar_expect_tx(bar(C::B_MFULL + st), mask_tx);
+#pragma unroll
+        for (int mb = 0; mb < BN / 64; ++mb)
+            tma_load_2d(smem_addr(sMask(st) + mb * C::MASK_BOX), &mp.mask, (t0 + i) * BN + mb * 64, 0,
+                        bar(C::B_MFULL + st));
+    };
+    // one producer thread feeds all three rings: first the slots every ring
+    // starts with, tile by tile
+    if (warp == kProdWarp && lane == 0) {
+        for (int i = 0; i < max(C::KS, max(C::VS, C::MS)) && i < n_my; ++i) {
+            if (i < C::KS) load_k(i);
+            if (a.has_mask && i < C::MS) load_m(i);
+            if (i < C::VS) load_v(i);
+        }
+    }
 
     // ---- prologue: the 128 Q rows as f16, SW128 K-major in every CTA --------
     // CTA rank c multicasts rows [c*R, (c+1)*R) to the cluster. When the rows
@@ -262,15 +295,44 @@ attn_tc_kernel(const __grid_constant__ TcArgs a, const __grid_constant__ Maps mp
     float m_ref = -INFINITY, l_part = 0.f;
     if (warp == kProdWarp) {
         if (lane == 0) {
-            for (int i = n_pre; i < n_my; ++i) {
-                wait(bar(C::B_EMPTY + i % C::STAGES), ((i / C::STAGES) - 1) & 1);
-                issue_load(i);
+            // Refill whichever slot frees first (non-blocking probes, K first: it
+            // gates the next S). No progress for the time limit = a timeout.
+            int nk = min(C::KS, n_my), nv = min(C::VS, n_my), nm = a.has_mask ? min(C::MS, n_my) : n_my;
+            uint64_t t_last = global_ns();
+            while (nk < n_my || nv < n_my || nm < n_my) {
+                bool moved = false;
+                if (nk < n_my && mbar_ready(bar(C::B_KEMPTY + nk % C::KS), ((nk / C::KS) - 1) & 1)) {
+                    load_k(nk++);
+                    moved = true;
+                }
+                if (nm < n_my && mbar_ready(bar(C::B_MEMPTY + nm % C::MS), ((nm / C::MS) - 1) & 1)) {
+                    load_m(nm++);
+                    moved = true;
+                }
+                if (nv < n_my && mbar_ready(bar(C::B_VEMPTY + nv % C::VS), ((nv / C::VS) - 1) & 1)) {
+                    load_v(nv++);
+                    moved = true;
+                }
+                if (moved) {
+                    t_last = global_ns();
+                } else {
+                    if (global_ns() - t_last > limit) {
+                        record_timeout(a.status, 1u);
+                        break;
+                    }
+                    __nanosleep(32);
+                }
             }
-            // drain: every issued load has landed before the stage memory is reused
+            // drain: every issued load has landed before the slot memory is reused
             // (full time limit even after a failure: no copy may outlive the CTA)
-            for (int i = max(0, n_my - C::STAGES); i < n_my; ++i)
-                if (!mbar_wait(bar(C::B_FULL + i % C::STAGES), (i / C::STAGES) & 1, limit))
-                    record_timeout(a.status, 1u);
+            for (int i = max(0, nk - C::KS); i < nk; ++i)
+                if (!mbar_wait(bar(C::B_KFULL + i % C::KS), (i / C::KS) & 1, limit)) record_timeout(a.status, 1u);
+            for (int i = max(0, nv - C::VS); i < nv; ++i)
+                if (!mbar_wait(bar(C::B_VFULL + i % C::VS), (i / C::VS) & 1, limit)) record_timeout(a.status, 1u);
+            if (a.has_mask)
+                for (int i = max(0, nm - C::MS); i < nm; ++i)
+                    if (!mbar_wait(bar(C::B_MFULL + i % C::MS), (i / C::MS) & 1, limit))
+                        record_timeout(a.status, 1u);
         }
     } else if (warp == kMmaWarp) {
         if (lane == 0) {
@@ -282,8 +344,8 @@ attn_tc_kernel(const __grid_constant__ TcArgs a, const __grid_constant__ Maps mp
             constexpr uint32_t idO = idesc_f16_f32(kRows, HD, 0, 1);
             const uint32_t q_base = smem_addr(sQ);
             auto issue_s = [&](int i) {
-                const int st = i % C::STAGES;
-                wait(bar(C::B_FULL + st), (i / C::STAGES) & 1);
+                const int st = i % C::KS;
+                wait(bar(C::B_KFULL + st), (i / C::KS) & 1);
                 tc_fence_after();
                 const uint32_t k_base = smem_addr(sK(st));
                 const uint32_t d = tbase + C::TM_S + (i & 1) * BN;
@@ -294,18 +356,20 @@ attn_tc_kernel(const __grid_constant__ TcArgs a, const __grid_constant__ Maps mp
                            sdesc_sw128(k_base + b * C::KV_BOX + off, 16, 1024), idS, kk > 0);
                 }
                 mma_commit(bar(C::B_SFULL + (i & 1)));
+                mma_commit(bar(C::B_KEMPTY + st));
             };
             // S_{i+1} goes ahead of PV_i only when its K tile has already landed, so
-            // PV_i (which frees a stage for the producer) never waits on a load.
+            // PV_i (which frees a V slot for the producer) never waits on a K load.
             int s_next = 0;
             if (n_my > 0) issue_s(s_next++);
             for (int i = 0; i < n_my; ++i) {
                 if (s_next == i + 1 && s_next < n_my &&
-                    mbar_test(bar(C::B_FULL + s_next % C::STAGES), (s_next / C::STAGES) & 1))
+                    mbar_ready(bar(C::B_KFULL + s_next % C::KS), (s_next / C::KS) & 1))
                     issue_s(s_next++);
                 wait(bar(C::B_PFULL + (i & 1)), (i >> 1) & 1);
+                wait(bar(C::B_VFULL + i % C::VS), (i / C::VS) & 1);
                 tc_fence_after();
-                const uint32_t v_base = smem_addr(sV(i % C::STAGES));
+                const uint32_t v_base = smem_addr(sV(i % C::VS));
                 const uint32_t p_tm = tbase + C::TM_P + (i & 1) * HB;
                 const uint32_t pl_tm = tbase + C::TM_PL + (i & 1) * HB;
 #pragma unroll
@@ -315,7 +379,7 @@ attn_tc_kernel(const __grid_constant__ TcArgs a, const __grid_constant__ Maps mp
                     mma_ts(tbase + C::TM_O, pl_tm + ks * 8, vd, idO, 1u);
                 }
                 mma_commit(bar(C::B_ODONE));
-                mma_commit(bar(C::B_EMPTY + i % C::STAGES));
+                mma_commit(bar(C::B_VEMPTY + i % C::VS));
                 if (s_next == i + 1 && s_next < n_my) issue_s(s_next++);
             }
             // drain: no MMA may still be running when TMEM is freed
@@ -340,7 +404,8 @@ attn_tc_kernel(const __grid_constant__ TcArgs a, const __grid_constant__ Maps mp
                 tmem_wait_ld();
                 const float kq = a.kq_log2;
                 if (a.has_mask) {
-                    const unsigned char* mk = sMask(i % C::STAGES);
+                    wait(bar(C::B_MFULL + i % C::MS), (i / C::MS) & 1);
+                    const unsigned char* mk = sMask(i % C::MS);
 #pragma unroll
                     for (int c8 = 0; c8 < HB / 8; ++c8) {
                         const int col = c_base + c8 * 8;
@@ -368,6 +433,10 @@ attn_tc_kernel(const __grid_constant__ TcArgs a, const __grid_constant__ Maps mp
 #pragma unroll
                 for (int c = 0; c < HB; ++c) pm4[c & 3] = fmaxf(pm4[c & 3], x[c]);
                 pm = fmaxf(fmaxf(pm4[0], pm4[1]), fmaxf(pm4[2], pm4[3]));
+            }
+            if (a.has_mask) {                     // this warp is done with mask slot i % MS
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(C::B_MEMPTY + i % C::MS));
             }
             sMaxX[((i & 1) * 2 + half) * kRows + r] = pm;
             quad_bar_sync(qd);
@@ -425,7 +494,7 @@ attn_tc_kernel(const __grid_constant__ TcArgs a, const __grid_constant__ Maps mp
     }
     __syncthreads();                    // every async load drained, every MMA done
     tc_fence_before();
-    cluster_sync();                     // #3: every CTA is done with its data region
+    if (CS > 1) cluster_sync();         // #3: every CTA is done with its data region
 
     if (a.merge_kernel) {
         // ---- merge-kernel mode: this split's (m, l, O) rows go to the workspace;
@@ -641,38 +710,42 @@ attn_tc_kernel(const __grid_constant__ TcArgs a, const __grid_constant__ Maps mp
 }
 
 // Merge of the split states written in merge-kernel mode. One CTA per (row,
-// 128-column chunk), 8 warps; warp w takes splits w, w+8, w+16, ... Every load
-// of a warp (its (m, l) pairs, one per lane, and its O chunks) is issued before
-// any is used. Each warp weighs its splits by 2^(m_s - m_w) against its own
-// maximum m_w; the 8 warp sums are then combined in warp order against the
-// row maximum. The order of every sum is fixed: the result does not depend on
+// 128-column chunk) of nw = min(kMergeWarps, splits) warps; warp w takes
+// splits w, w + nw, ... (at most a handful each, so the loads of the whole CTA
+// are in flight together). Each warp weighs its splits by 2^(m_s - m_w) against its own
+// maximum m_w; the warp sums are then combined in warp order against the row
+// maximum. The order of every sum is fixed: the result does not depend on
 // timing.
+constexpr int kMergeWarps = 32;
+
 template <int HD>
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(kMergeWarps * 32)
 attn_merge_kernel(const float* __restrict__ part_o, const float2* __restrict__ part_ml, float* __restrict__ out,
                   int M, int splits) {
     constexpr int CWM = HD < 128 ? HD : 128;
     constexpr int NCH = HD / CWM;
     constexpr int LANES = CWM / 4;
-    constexpr int PER_WARP = (kMaxMergeSplits + 7) / 8;
+    constexpr int PER_WARP = (kMaxMergeSplits + kMergeWarps - 1) / kMergeWarps;
     static_assert(PER_WARP <= 32, "one (m, l) pair per lane");
-    __shared__ float s_acc[8][CWM];
-    __shared__ float s_m[8], s_l[8];
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    __shared__ float s_acc[kMergeWarps][CWM];
+    __shared__ float s_m[kMergeWarps], s_l[kMergeWarps];
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, nw = (int)(blockDim.x >> 5);
     const int row = blockIdx.x / NCH, chunk = blockIdx.x - row * NCH;
     const int rt = row >> 7, rr = row & 127;
     asm volatile("griddepcontrol.wait;" ::: "memory");     // the attention grid is complete
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    const int n_w = splits > warp ? (splits - warp + 7) / 8 : 0;   // splits of this warp
+    const int n_w = splits > warp ? (splits - warp + nw - 1) / nw : 0;   // this warp's splits
     const float2* ml = part_ml + (int64_t)rt * splits * kRows + rr;
-    const float2 my_ml = lane < n_w ? __ldcg(ml + (int64_t)(warp + 8 * lane) * kRows) : make_float2(-INFINITY, 0.f);
+    const float2 my_ml =
+        lane < n_w ? __ldcg(ml + (int64_t)(warp + nw * lane) * kRows) : make_float2(-INFINITY, 0.f);
     float4 v[PER_WARP];
     const float* base = part_o + ((int64_t)rt * splits * kRows + rr) * HD + chunk * CWM + (lane % LANES) * 4;
     const int64_t sstride = (int64_t)kRows * HD;
 #pragma unroll
     for (int u = 0; u < PER_WARP; ++u)
-        v[u] = (u < n_w && lane < LANES) ? __ldcg(reinterpret_cast<const float4*>(base + (warp + 8 * u) * sstride))
-                                         : make_float4(0.f, 0.f, 0.f, 0.f);
+        v[u] = (u < n_w && lane < LANES)
+                   ? __ldcg(reinterpret_cast<const float4*>(base + (warp + nw * u) * sstride))
+                   : make_float4(0.f, 0.f, 0.f, 0.f);
     float mw = my_ml.x;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) mw = fmaxf(mw, __shfl_xor_sync(0xffffffffu, mw, o));
@@ -696,19 +769,20 @@ attn_merge_kernel(const float* __restrict__ part_o, const float2* __restrict__ p
         s_l[warp] = lw;
     }
     __syncthreads();
-    if (tid < CWM && row < M) {
+    if (row < M) {
         float mx = -INFINITY;
-#pragma unroll
-        for (int w = 0; w < 8; ++w) mx = fmaxf(mx, s_m[w]);
+        for (int w = 0; w < nw; ++w) mx = fmaxf(mx, s_m[w]);
         const float mref = mx == -INFINITY ? 0.f : mx;
-        float sum = 0.f, L = 0.f;
-#pragma unroll
-        for (int w = 0; w < 8; ++w) {
-            const float sc = s_m[w] == -INFINITY ? 0.f : ex2(s_m[w] - mref);
-            sum = fmaf(sc, s_acc[w][tid], sum);
-            L = fmaf(sc, s_l[w], L);
+        for (int c = tid; c < CWM; c += blockDim.x) {      // fewer threads than columns when nw < 4
+            float sum = 0.f, L = 0.f;
+#pragma unroll 4
+            for (int w = 0; w < nw; ++w) {
+                const float sc = s_m[w] == -INFINITY ? 0.f : ex2(s_m[w] - mref);
+                sum = fmaf(sc, s_acc[w][c], sum);
+                L = fmaf(sc, s_l[w], L);
+            }
+            out[(int64_t)row * HD + chunk * CWM + c] = L > 0.f ? sum / L : 0.f;
         }
-        out[(int64_t)row * HD + chunk * CWM + tid] = L > 0.f ? sum / L : 0.f;
     }
 }
 
@@ -719,7 +793,7 @@ fr_status launch_merge(const float* part_o, const float2* part_ml, float* out, i
     memset(&cfg, 0, sizeof(cfg));
     const int nch = hd < 128 ? 1 : hd / 128;
     cfg.gridDim = dim3(M * nch, 1, 1);
-    cfg.blockDim = dim3(256, 1, 1);
+    cfg.blockDim = dim3((splits < kMergeWarps ? splits : kMergeWarps) * 32, 1, 1);
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
