@@ -368,7 +368,7 @@ def run_ours(args, rank, world, local_rank):
         "kv_gbs": kv_real_bytes / (us_per_call * 1e-6) / 1e9,
         "kv_frac_of_hbm": kv_real_bytes / (us_per_call * 1e-6) / 1e9 / peak,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "traffic": ncu_traffic(args.config),
+                     "frac": achieved / peak, "traffic": ncu_traffic(w.name),
                      "peak_kind": f"{peak_kind} hbm_gbs (burst copy)",
                      "kernel": f"{attn_kernels} (decode attention on f16 Q rows, one call)",
                      "kernel_us_per_launch": attn_us,
