@@ -10,8 +10,9 @@ Prints ONE JSON line (rank 0). `value` is device time per call in µs (lower is
 better), measured with CUDA events around K back-to-back calls replayed from a
 CUDA graph, with K/V, Q and mask rotated over replicas whose total exceeds
 2x L2, so every call streams its K/V from HBM. `e2e` is the same call made
-through the public API with pinned host buffers: host->device copies of that
-step's inputs and a device->host read of its output inside the timed region.
+through the public API with pinned host buffers: the step's inputs (q, pos,
+K, V, mask) packed in one pinned block and copied host->device in one copy,
+and a device->host read of its output, all inside the timed region.
 
 `--impl reference` times the plain fp64 CPU oracle on the host cores on the
 same workload (each step = one oracle call), for the driver's ratio.
@@ -164,6 +165,22 @@ def cpu_oracle_time(config, budget_s, threads=1):
     return d["us"], d["calls"]
 
 
+def max_over_ranks(x, dist, device):
+    """Largest value of x over all ranks (x itself without a process group)."""
+    if dist is None:
+        return float(x)
+    import torch
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_calls_per_s(world, steps, ms_max):
+    """Calls per second of the whole job: every rank runs `steps` calls, the
+    slowest rank's time bounds the job."""
+    return world * steps / (ms_max / 1000.0)
+
+
 def run_reference(args, rank, world):
     """The CPU oracle as the reference arm."""
     import gen
@@ -309,38 +326,56 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.synchronize()
     if dist:
         dist.barrier()
-    ms = ev0.elapsed_time(ev1)
-    if dist:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ev0.elapsed_time(ev1), dist, dev)
     us_per_call = ms * 1000.0 / args.steps
 
     # --- end to end through the public API with pinned host buffers ----------
-    q_p = q_h.pin_memory(); pos_p = pos_h.pin_memory(); k_p = k_h.pin_memory(); v_p = v_h.pin_memory()
-    m_p = None if m_h is None else m_h.pin_memory()
+    # The step's inputs travel as one packed block (each tensor 256-byte
+    # aligned inside it): one host-to-device copy in, one device-to-host copy of
+    # out back, the fused call on views of the device block in between.
+    parts = [("q", q_h), ("pos", pos_h), ("k", k_h), ("v", v_h)] + ([("mask", m_h)] if m_h is not None else [])
+    offs, total = {}, 0
+    for name, t in parts:
+        total = (total + 255) // 256 * 256
+        offs[name] = (total, t.numel() * t.element_size())
+        total += t.numel() * t.element_size()
+    host_pack = torch.empty(total, dtype=torch.uint8).pin_memory()
+    for name, t in parts:
+        o, n = offs[name]
+        host_pack[o:o + n].copy_(t.contiguous().view(-1).view(torch.uint8))
+    def device_views(buf):
+        return {name: buf[offs[name][0]:offs[name][0] + offs[name][1]].view(t.dtype).view(t.shape)
+                for name, t in parts}
+    packs = [torch.empty(total, dtype=torch.uint8, device=dev) for _ in range(2)]
+    pack_views = [device_views(b) for b in packs]
+    for pv in pack_views:
+        pv.setdefault("mask", None)
     out_p = torch.empty(out.shape, dtype=torch.float32).pin_memory()
     e2e_steps = min(args.steps, 200)
-    h2d = sum(t.numel() * t.element_size() for t in (q_p, pos_p, k_p, v_p) + ((m_p,) if m_p is not None else ()))
+    h2d = total
     d2h = out_p.numel() * 4
-    def e2e_step(r):
-        r["q"].copy_(q_p, non_blocking=True); r["pos"].copy_(pos_p, non_blocking=True)
-        r["k"].copy_(k_p, non_blocking=True); r["v"].copy_(v_p, non_blocking=True)
-        if m_p is not None:
-            r["mask"].copy_(m_p, non_blocking=True)
-        call(r, stream)
+    def e2e_step(i):
+        packs[i % 2].copy_(host_pack, non_blocking=True)
+        call(pack_views[i % 2], stream)
         out_p.copy_(out, non_blocking=True)
     with torch.cuda.stream(stream):
         for i in range(3):
-            e2e_step(reps[i % n_rep])
+            e2e_step(i)
         stream.synchronize()
         e0 = torch.cuda.Event(enable_timing=True); e1 = torch.cuda.Event(enable_timing=True)
         e0.record(stream)
         for i in range(e2e_steps):
-            e2e_step(reps[i % n_rep])
+            e2e_step(i)
         e1.record(stream)
     stream.synchronize()
-    e2e_us = e0.elapsed_time(e1) * 1000.0 / e2e_steps
+    e2e_us = max_over_ranks(e0.elapsed_time(e1) * 1000.0 / e2e_steps, dist, dev)
+    # the packed inputs give the same result as the inputs the timed graph used
+    ref_out = out.clone()
+    with torch.cuda.stream(stream):
+        call(reps[0], stream)
+    stream.synchronize()
+    if not torch.equal(ref_out, out):
+        raise RuntimeError("end-to-end call on packed inputs differs from the direct call")
 
     # --- CPU oracle baseline (rank 0 only, N = 1 only) -------------------------
     cpu = None
@@ -365,6 +400,7 @@ def run_ours(args, rank, world, local_rank):
                    "plan": plan,
                    "l2": f"inputs rotated over {n_rep} replicas ({n_rep * per_rep / 2**20:.0f} MiB > 2x L2)",
                    "parallelism": "replicas only" if world > 1 else "1 GPU"},
+        "calls_per_s_all_ranks": job_calls_per_s(world, args.steps, ms),
         "kv_gbs": kv_real_bytes / (us_per_call * 1e-6) / 1e9,
         "kv_frac_of_hbm": kv_real_bytes / (us_per_call * 1e-6) / 1e9 / peak,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
