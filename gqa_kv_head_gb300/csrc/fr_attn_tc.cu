@@ -67,6 +67,8 @@ constexpr int kThreads = (kSmaxWarps + 2) * 32;
 constexpr float kTau = 8.0f;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr uint32_t kTmemCols = 512;
+constexpr int kOutBoxRows = 32;              // rows per TMA store box of the split states
+static_assert(kRows % kOutBoxRows == 0 && kOutBoxRows % 8 == 0, "whole 128-byte swizzle periods per box");
 
 template <int HD>
 struct Cfg {
@@ -528,9 +530,15 @@ attn_tc_kernel(const __grid_constant__ TcArgs a, const __grid_constant__ Maps mp
             fence_proxy_async_cta();        // the boxes are read by the TMA engine
             softmax_bar_sync();
             if (warp == 0 && lane == 0) {
+                // only the 32-row blocks that hold real rows
                 const int y = (rt * a.splits + split) * kRows;
+                const int n_rb = (rows_real + kOutBoxRows - 1) / kOutBoxRows;
 #pragma unroll 1
-                for (int bx = 0; bx < HD / 32; ++bx) tma_store_2d(&mp.po, bx * 32, y, smem_addr(sOut + bx * C::OBOX));
+                for (int rb = 0; rb < n_rb; ++rb)
+#pragma unroll 1
+                    for (int bx = 0; bx < HD / 32; ++bx)
+                        tma_store_2d(&mp.po, bx * 32, y + rb * kOutBoxRows,
+                                     smem_addr(sOut + bx * C::OBOX + rb * kOutBoxRows * 128));
                 bulk_commit();
                 bulk_wait_all();            // performed before the grid completes
             }
@@ -876,7 +884,7 @@ static fr_status launch(const TcLaunch& L, cudaStream_t stream) {
     if (a.has_mask && !encode_2d(&mp.mask, L.mask, a.n_kv, a.n_tok, L.m_rs, 64, a.n_tok)) return FR_ERR_CUDA;
     if (!a.q16 || !encode_2d(&mp.q16, a.q16, HD, a.M, HD, 64, kRows / a.C)) return FR_ERR_CUDA;
     if (a.merge_kernel &&
-        !encode_2d_f32(&mp.po, a.part_o, HD, (uint64_t)L.row_tiles * a.splits * kRows, kRows))
+        !encode_2d_f32(&mp.po, a.part_o, HD, (uint64_t)L.row_tiles * a.splits * kRows, kOutBoxRows))
         return FR_ERR_CUDA;
 
     cudaLaunchConfig_t cfg;
