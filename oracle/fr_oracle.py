@@ -123,6 +123,35 @@ def qkv_post(q, pos, rp, q_scale):
     return rows, f16_round(rows)
 
 
+def kv_append(k_cache, v_cache, k_new, v_new, pos, rp, row0, pad=None):
+    """The K/V leg of qkv_post with the write of the new rows into the
+    persistent KV cache (FlashRT PR #185, commit "Fuses the prefix layers'
+    q/k/v projections, RoPE, scale, KV padding to the FA KQ stride, and the
+    permuted f16 materializations ..."; the full variant "re-emits the rope'd K
+    and plain V as f32 rows" and "pad rows are zeroed").
+
+    The new K rows are rotated exactly as the Q rows of the same tokens (same
+    angles and mscale, no 1/sqrt(hd) scale); K and V are rounded once to f16
+    and written at cache rows row0 + t. pad = (begin, end) rows of both caches
+    are set to zero (the attention reads a padded length). Nothing else changes.
+
+    k_cache, v_cache: f16 [n_ctx, hd]; k_new, v_new: [n_tok, hd]; pos: [n_tok].
+    Returns (k_cache', v_cache', k_rope fp64 [n_tok, hd], v fp64 [n_tok, hd]).
+    """
+    k_new = np.asarray(k_new, dtype=np.float64)
+    v_new = np.asarray(v_new, dtype=np.float64)
+    n_tok = k_new.shape[0]
+    k_rope = rope_neox(k_new[:, None, :], pos, rp)[:, 0, :]
+    kc = np.array(k_cache, dtype=np.float16, copy=True)
+    vc = np.array(v_cache, dtype=np.float16, copy=True)
+    kc[row0:row0 + n_tok] = f16_round(k_rope)
+    vc[row0:row0 + n_tok] = f16_round(v_new)
+    if pad is not None:
+        kc[pad[0]:pad[1]] = 0
+        vc[pad[0]:pad[1]] = 0
+    return kc, vc, k_rope, v_new
+
+
 # ---------------------------------------------------------------------------
 # Attention over one shared KV head
 # ---------------------------------------------------------------------------

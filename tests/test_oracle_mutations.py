@@ -27,6 +27,12 @@ MUTANTS = {
     "head_major_rows": ("rows = y.reshape(n_tok * n_head, hd)",
                         "rows = y.transpose(1, 0, 2).reshape(n_tok * n_head, hd)"),
     "dropped_q_scale": ("y = rope_neox(q, pos, rp) * float(q_scale)", "y = rope_neox(q, pos, rp)"),
+    "k_scaled_like_q": ("k_rope = rope_neox(k_new[:, None, :], pos, rp)[:, 0, :]",
+                        "k_rope = rope_neox(k_new[:, None, :], pos, rp)[:, 0, :] / math.sqrt(k_new.shape[1])"),
+    "k_rotated_backwards": ("k_rope = rope_neox(k_new[:, None, :], pos, rp)[:, 0, :]",
+                            "k_rope = rope_neox(k_new[:, None, :], -np.asarray(pos), rp)[:, 0, :]"),
+    "tail_off_by_one": ("kc[row0:row0 + n_tok] = f16_round(k_rope)", "kc[row0 + 1:row0 + 1 + n_tok] = f16_round(k_rope)"),
+    "pad_not_zeroed": ("        kc[pad[0]:pad[1]] = 0\n", ""),
 }
 
 
@@ -40,6 +46,7 @@ def test_pins_catch_mutant(name, tmp_path):
     env = dict(os.environ, FR_ORACLE_MUTANT=str(mut))
     r = subprocess.run([sys.executable, "-m", "pytest", "-q", "-x", "-p", "no:cacheprovider",
                         os.path.join(HERE, "test_oracle_rope.py"),
-                        os.path.join(HERE, "test_oracle_attn.py")],
+                        os.path.join(HERE, "test_oracle_attn.py"),
+                        os.path.join(HERE, "test_oracle_kv.py")],
                        env=env, capture_output=True, text=True, cwd=os.path.dirname(HERE))
     assert r.returncode != 0, f"mutant {name} survived the oracle pins:\n{r.stdout[-2000:]}"
