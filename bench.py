@@ -297,6 +297,35 @@ def run_ours(args, rank, world, local_rank):
     stream.synchronize()
     attn_us = ka0.elapsed_time(ka1) * 1000.0 / (n_attn * G)
 
+    # the K/V leg of qkv_post (the next layer of the path, timed beside it, not
+    # part of `value`): n_tok new rows appended at the tail of each replica's
+    # cache, pad rows zeroed
+    kv_new = {"k": torch.randn((w.n_tok, w.hd), device=dev), "v": torch.randn((w.n_tok, w.hd), device=dev)}
+    row0 = w.n_kv_real - w.n_tok
+    pad = (w.n_kv_real, w.n_kv) if w.n_kv_real < w.n_kv else None
+    kv_caches = [(torch.empty_like(r["k"]).copy_(r["k"]), torch.empty_like(r["v"]).copy_(r["v"]))
+                 for r in reps[:2]]
+    def call_kv(i, st):
+        kc, vc = kv_caches[i % 2]
+        fr.kv_append(kv_new["k"], kv_new["v"], reps[0]["pos"], w.rope, kc, vc, row0, pad=pad, stream=st)
+    with torch.cuda.stream(stream):
+        for i in range(3):
+            call_kv(i, stream)
+    stream.synchronize()
+    g_kv = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_kv, stream=stream):
+        for i in range(G):
+            call_kv(i, stream)
+    with torch.cuda.stream(stream):
+        g_kv.replay()
+        kv0 = torch.cuda.Event(enable_timing=True); kv1 = torch.cuda.Event(enable_timing=True)
+        kv0.record(stream)
+        g_kv.replay()
+        kv1.record(stream)
+    stream.synchronize()
+    kv_append_us = kv0.elapsed_time(kv1) * 1000.0 / G
+    del kv_caches
+
     dist = None
     if world > 1:
         import torch.distributed as dist
@@ -412,6 +441,7 @@ def run_ours(args, rank, world, local_rank):
         "e2e": {"value": e2e_us, "unit": "us/call", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
         "gpu_launches": plan["launches"] * args.steps,
+        "kv_append_us": kv_append_us,
         "clocks": clk,
     }
     if cpu is not None:

@@ -127,9 +127,111 @@ fr_status launch_qkv_post(const float* q, int64_t q_tok_stride, const int32_t* p
     return e == cudaSuccess ? FR_OK : FR_ERR_CUDA;
 }
 
+// K/V leg: one grid-stride pass over three kinds of work item — rotated K
+// pairs (the same device routine as the Q rows, scale 1), groups of 8 V
+// elements (one 16-byte f16 store) and 16-byte zero stores of the pad rows.
+template <int HD>
+__global__ void __launch_bounds__(256)
+kv_append_kernel(const float* __restrict__ k_new, int64_t k_stride, const float* __restrict__ v_new,
+                 int64_t v_stride, const int32_t* __restrict__ pos, int n_tok, __half* __restrict__ k_cache,
+                 int64_t k_rs, __half* __restrict__ v_cache, int64_t v_rs, int64_t row0, int64_t pad_begin,
+                 int64_t pad_rows, float* __restrict__ k32, float* __restrict__ v32,
+                 const __grid_constant__ RopeTable tb) {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    constexpr int G = HD / 8;                                  // 8-element groups per row
+    const int64_t nK = (int64_t)n_tok * (HD / 2), nV = (int64_t)n_tok * G, nP = pad_rows * G;
+    for (int64_t w = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; w < nK + nV + nP;
+         w += (int64_t)gridDim.x * blockDim.x) {
+        if (w < nK) {
+            const int t = (int)(w / (HD / 2)), c = (int)(w - (int64_t)t * (HD / 2));
+            int d0, d1;
+            float y0, y1;
+            rope_slot(k_new + (int64_t)t * k_stride, c, __ldg(pos + t), tb, d0, d1, y0, y1);
+            __half* krow = k_cache + (row0 + t) * k_rs;
+            krow[d0] = __float2half_rn(y0);
+            krow[d1] = __float2half_rn(y1);
+            if (k32) {
+                k32[(int64_t)t * HD + d0] = y0;
+                k32[(int64_t)t * HD + d1] = y1;
+            }
+        } else if (w < nK + nV) {
+            const int64_t u = w - nK;
+            const int t = (int)(u / G), g = (int)(u - (int64_t)t * G);
+            const float4* src = reinterpret_cast<const float4*>(v_new + (int64_t)t * v_stride + g * 8);
+            const float4 a = src[0], b = src[1];
+            uint4 h;
+            h.x = pack_half2(a.x, a.y);
+            h.y = pack_half2(a.z, a.w);
+            h.z = pack_half2(b.x, b.y);
+            h.w = pack_half2(b.z, b.w);
+            *reinterpret_cast<uint4*>(v_cache + (row0 + t) * v_rs + g * 8) = h;
+            if (v32) {
+                float4* dst = reinterpret_cast<float4*>(v32 + (int64_t)t * HD + g * 8);
+                dst[0] = a;
+                dst[1] = b;
+            }
+        } else {
+            const int64_t u = w - nK - nV;
+            const int64_t row = pad_begin + u / G;
+            const int g = (int)(u % G);
+            const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+            *reinterpret_cast<uint4*>(k_cache + row * k_rs + g * 8) = z;
+            *reinterpret_cast<uint4*>(v_cache + row * v_rs + g * 8) = z;
+        }
+    }
+}
+
 }  // namespace fr
 
 using namespace fr;
+
+extern "C" fr_status fr_kv_append(const float* k_new, int64_t k_stride, const float* v_new, int64_t v_stride,
+                                  const int32_t* pos, int n_tok, int hd, const fr_rope_params* rp,
+                                  uint16_t* k_cache, int64_t k_row_stride, uint16_t* v_cache,
+                                  int64_t v_row_stride, int64_t n_ctx, int64_t row0, int64_t pad_begin,
+                                  int64_t pad_end, float* k32_out, float* v32_out, cudaStream_t stream) {
+    if (!k_new || !v_new || !pos || !rp || !k_cache || !v_cache) return FR_ERR_INVALID_ARG;
+    if (n_tok < 1 || hd < 1) return FR_ERR_INVALID_ARG;
+    if (hd != 64 && hd != 128 && hd != 256) return FR_ERR_UNSUPPORTED;
+    if (n_tok > kMaxTok) return FR_ERR_UNSUPPORTED;
+    if (k_stride < hd || (k_stride & 3) || v_stride < hd || (v_stride & 3)) return FR_ERR_INVALID_ARG;
+    if (k_row_stride < hd || (k_row_stride & 7) || v_row_stride < hd || (v_row_stride & 7))
+        return FR_ERR_INVALID_ARG;
+    if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(k_cache) || !aligned16(v_cache) ||
+        (k32_out && !aligned16(k32_out)) || (v32_out && !aligned16(v32_out)))
+        return FR_ERR_INVALID_ARG;
+    if (row0 < 0 || row0 + n_tok > n_ctx) return FR_ERR_INVALID_ARG;            // tail inside the cache
+    if (pad_begin < 0 || pad_end < pad_begin || pad_end > n_ctx) return FR_ERR_INVALID_ARG;
+    if (pad_end > pad_begin && pad_begin < row0 + n_tok && row0 < pad_end) return FR_ERR_INVALID_ARG;
+    RopeTable tb;
+    if (!build_rope_table(rp, 1.0f, hd, &tb)) return FR_ERR_INVALID_ARG;
+    const int64_t total = (int64_t)n_tok * (hd / 2) + ((int64_t)n_tok + (pad_end - pad_begin)) * (hd / 8);
+    const int blocks = (int)(total < 256 * 1184 ? (total + 255) / 256 : 1184);
+    cudaLaunchConfig_t cfg;
+    memset(&cfg, 0, sizeof(cfg));
+    cfg.gridDim = dim3(blocks);
+    cfg.blockDim = dim3(256);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    __half* kc = reinterpret_cast<__half*>(k_cache);
+    __half* vc = reinterpret_cast<__half*>(v_cache);
+    const int64_t pr = pad_end - pad_begin;
+    cudaError_t e;
+    switch (hd) {
+        case 64: e = cudaLaunchKernelEx(&cfg, kv_append_kernel<64>, k_new, k_stride, v_new, v_stride, pos, n_tok, kc,
+                                        k_row_stride, vc, v_row_stride, row0, pad_begin, pr, k32_out, v32_out, tb); break;
+        case 128: e = cudaLaunchKernelEx(&cfg, kv_append_kernel<128>, k_new, k_stride, v_new, v_stride, pos, n_tok, kc,
+                                         k_row_stride, vc, v_row_stride, row0, pad_begin, pr, k32_out, v32_out, tb); break;
+        default: e = cudaLaunchKernelEx(&cfg, kv_append_kernel<256>, k_new, k_stride, v_new, v_stride, pos, n_tok, kc,
+                                        k_row_stride, vc, v_row_stride, row0, pad_begin, pr, k32_out, v32_out, tb); break;
+    }
+    return e == cudaSuccess ? FR_OK : FR_ERR_CUDA;
+}
 
 extern "C" const char* fr_status_string(fr_status s) {
     switch (s) {

@@ -71,6 +71,34 @@ def qkv_post(q, pos, n_head, hd, rope, q_scale=None, q16_out=None, q32_out=None,
     return q16_out, q32_out
 
 
+def kv_append(k_new, v_new, pos, rope, k_cache, v_cache, row0, pad=None, k32_out=None, v32_out=None,
+              stream=None):
+    """fr_kv_append: rope the new K rows, round K and V to f16 and write them at
+    cache rows row0 .. row0 + n_tok - 1; zero the pad rows (pad = (begin, end)).
+    k_new, v_new: f32 [n_tok, hd] (row stride may exceed hd, e.g. columns of a
+    fused QKV buffer); k_cache, v_cache: f16 [n_ctx, hd] (row stride >= hd)."""
+    lib = _abi.load()
+    _check_dev(k_new, v_new, pos, k_cache, v_cache, k32_out, v32_out)
+    for name, t in (("k_new", k_new), ("v_new", v_new), ("k32_out", k32_out), ("v32_out", v32_out)):
+        if t is not None and t.dtype != torch.float32:
+            raise TypeError(f"{name} must be float32")
+    for name, t in (("k_cache", k_cache), ("v_cache", v_cache)):
+        if t.dtype != torch.float16:
+            raise TypeError(f"{name} must be float16")
+    if pos.dtype != torch.int32:
+        raise TypeError("pos must be int32")
+    n_tok, hd = k_new.shape[0], k_new.shape[1]
+    if tuple(v_new.shape) != (n_tok, hd) or k_cache.shape[1] != hd or tuple(v_cache.shape) != tuple(k_cache.shape):
+        raise ValueError("shape mismatch")
+    pb, pe = pad if pad is not None else (0, 0)
+    rp = _as_rope(rope)
+    st = lib.fr_kv_append(_ptr(k_new), _row_stride(k_new, "k_new"), _ptr(v_new), _row_stride(v_new, "v_new"),
+                          _ptr(pos), n_tok, hd, ctypes.byref(rp), _ptr(k_cache), _row_stride(k_cache, "k_cache"),
+                          _ptr(v_cache), _row_stride(v_cache, "v_cache"), k_cache.shape[0], int(row0), int(pb),
+                          int(pe), _ptr(k32_out), _ptr(v32_out), _stream(stream))
+    _abi.check(st, "fr_kv_append")
+
+
 def workspace_size(n_tok, n_head, hd, n_kv):
     return int(_abi.load().fr_decode_attn_workspace_size(n_tok, n_head, hd, n_kv))
 

@@ -107,6 +107,40 @@ fr_status fr_qkv_post(const float* q, int64_t q_tok_stride, const int32_t* pos,
                       uint16_t* q16_out, float* q32_out, cudaStream_t stream);
 
 /*
+ * fr_kv_append -- the K/V leg of qkv_post with the write of the new rows into
+ * the persistent KV cache (FlashRT PR #185, commit "Fuses the prefix layers'
+ * q/k/v projections, RoPE, scale, KV padding to the FA KQ stride, and the
+ * permuted f16 materializations ..."; its full variant re-emits the rope'd K
+ * and plain V as f32 rows and zeroes the pad rows).
+ *
+ * For each new token t < n_tok:
+ *   k_cache[row0 + t] = f16_RN(mscale * NEOX-RoPE(k_new[t], pos[t]))   no 1/sqrt(hd)
+ *   v_cache[row0 + t] = f16_RN(v_new[t])
+ * with the same angles, YaRN terms and fp32 arithmetic as fr_qkv_post's Q rows,
+ * and rows [pad_begin, pad_end) of both caches set to zero. No other row is
+ * touched.
+ *
+ *   k_new, v_new  f32, row t at k_new + t*k_stride (elements, >= hd, multiple
+ *                 of 4), hd contiguous values — e.g. the K and V columns of a
+ *                 fused QKV GEMM output.
+ *   k_cache, v_cache  f16 [n_ctx][hd], row strides >= hd, multiples of 8.
+ *   row0          first cache row written; [row0, row0 + n_tok) and
+ *                 [pad_begin, pad_end) must lie in [0, n_ctx) and not overlap.
+ *   k32_out, v32_out  optional f32 [n_tok][hd] copies (rope'd K, plain V).
+ * All pointers 16-byte aligned. Launched with programmatic stream
+ * serialization; the kernel waits for the grids before it on the stream
+ * before reading. A following fr_decode_attn on the same stream sees the new
+ * rows: its qkv_post kernel waits for this grid before it releases the
+ * attention launch.
+ * Supported: 1 <= n_tok <= 16, hd in {64, 128, 256}.
+ */
+fr_status fr_kv_append(const float* k_new, int64_t k_stride, const float* v_new, int64_t v_stride,
+                       const int32_t* pos, int n_tok, int hd, const fr_rope_params* rp,
+                       uint16_t* k_cache, int64_t k_row_stride, uint16_t* v_cache, int64_t v_row_stride,
+                       int64_t n_ctx, int64_t row0, int64_t pad_begin, int64_t pad_end,
+                       float* k32_out, float* v32_out, cudaStream_t stream);
+
+/*
  * Workspace bytes for this shape that admit every plan of fr_decode_attn,
  * the separate merge kernel's included (0 for unsupported shapes). The
  * workspace holds the split-KV partial states, self-resetting arrival tickets

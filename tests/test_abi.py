@@ -137,6 +137,30 @@ def test_workspace_size_covers_the_merge_kernel_plan(lib):
         assert ws(n_tok, n_head, hd, 1024) >= (160 // rt) * rt * 128 * (hd * 4 + 8)
 
 
+def test_kv_append_validation(lib):
+    rp = _rope(lib)
+    def call(k=FAKE, v=FAKE, pos=FAKE, n_tok=4, hd=128, ks=128, kr=128, n_ctx=64, row0=10, pb=40, pe=64,
+             k32=None, rp_=rp):
+        return lib.fr_kv_append(k, ks, v, 128, pos, n_tok, hd, ctypes.byref(rp_), FAKE, kr, FAKE, 128,
+                                n_ctx, row0, pb, pe, k32, None, None)
+    assert call(k=None) == 1
+    assert call(pos=None) == 1
+    assert call(hd=96) == 2
+    assert call(n_tok=17) == 2
+    assert call(ks=100) == 1                 # f32 row stride not a multiple of 4
+    assert call(ks=64) == 1                  # stride < hd
+    assert call(kr=132) == 1                 # f16 row stride not a multiple of 8
+    assert call(k=MIS) == 1                  # misaligned
+    assert call(k32=MIS) == 1
+    assert call(row0=62) == 1                # tail past n_ctx
+    assert call(row0=-1) == 1
+    assert call(pb=12, pe=20) == 1           # pad overlaps the tail rows
+    assert call(pe=65) == 1                  # pad past n_ctx
+    assert call(pb=30, pe=20) == 1
+    from gqa_kv_head_gb300 import rope_params
+    assert call(rp_=rope_params(127)) == 1   # odd n_dims
+
+
 def test_workspace_init_rejects_null(lib):
     assert lib.fr_workspace_init(None, 4096, None) == 1
     assert lib.fr_workspace_check(None, None) == 1
