@@ -154,6 +154,11 @@ def named_config(name, seed=0):
                                         beta_fast=32.0, beta_slow=1.0, n_ctx_orig=4096),
                         positions=_tail_positions(32768, 16), mask_kind="causal",
                         outlier_p=0.01, outlier_mult=20.0, seed=seed)
+    if name == "pi05_prefill":
+        # the prefix window: KV length = query count, pad-only (prefix-LM) mask
+        return Workload("pi05_prefill", n_head=8, n_tok=968, hd=256, n_kv=1024, n_kv_real=968,
+                        rope=RopeParams(n_dims=256, freq_base=10000.0),
+                        positions=tuple(range(968)), mask_kind="none", kv_sigma=0.5, seed=seed)
     raise KeyError(name)
 
 

@@ -28,6 +28,7 @@ struct TcArgs {
     int n_clusters;           // clusters per row tile
     int C;                    // CTAs per cluster (splits per cluster)
     int merge_kernel;         // 1: write every split's state for attn_merge_kernel (C == 1)
+    int early_dep;            // 1: the grid is one wave; a dependent launch may start after set-up
     int splits;               // splits per row tile
     float kq_log2;
     uint64_t wait_limit_ns;

@@ -230,13 +230,19 @@ attn_tc_kernel(const __grid_constant__ TcArgs a, const __grid_constant__ Maps mp
     else __syncthreads();               //     (one-CTA cluster: a CTA barrier is enough)
     tc_fence_after();
     const uint32_t tbase = *sTmemBase;
-    // a dependent merge grid (merge-kernel mode) may be scheduled now; it waits
-    // for this grid's completion before reading the split states
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    // a dependent grid (the merge kernel, or the next call's qkv_post) may be
+    // scheduled now; it waits for this grid's completion before reading what it
+    // writes. Only when this grid is one wave: otherwise waiting dependent CTAs
+    // could hold SMs that later CTAs of this grid need.
+    if (a.early_dep) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
     // K/V/mask tiles need no Q: the first ones are requested before the
     // prologue.
-    const uint32_t mask_tx = a.has_mask ? (uint32_t)(BN / 64) * 128u * (uint32_t)a.n_tok : 0u;
+    // mask rows: all tokens when n_tok <= kMaskWin, else the kMaskWin tokens
+    // from this row tile's first one (they hold every token of the tile)
+    const int mask_rows = min(a.n_tok, kMaskWin);
+    const int mask_t0 = a.n_tok <= kMaskWin ? 0 : row0 / a.n_head;
+    const uint32_t mask_tx = a.has_mask ? (uint32_t)(BN / 64) * 128u * (uint32_t)mask_rows : 0u;
     auto load_k = [&](int i) {
         const int st = i % C::KS;
         mbar_expect_tx(bar(C::B_KFULL + st), (uint32_t)C::K_BYTES);
@@ -256,7 +262,7 @@ attn_tc_kernel(const __grid_constant__ TcArgs a, const __grid_constant__ Maps mp
         mbar_expect_tx(bar(C::B_MFULL + st), mask_tx);
 #pragma unroll
         for (int mb = 0; mb < BN / 64; ++mb)
-            tma_load_2d(smem_addr(sMask(st) + mb * C::MASK_BOX), &mp.mask, (t0 + i) * BN + mb * 64, 0,
+            tma_load_2d(smem_addr(sMask(st) + mb * C::MASK_BOX), &mp.mask, (t0 + i) * BN + mb * 64, mask_t0,
                         bar(C::B_MFULL + st));
     };
     // one producer thread feeds all three rings: first the slots every ring
@@ -393,7 +399,7 @@ attn_tc_kernel(const __grid_constant__ TcArgs a, const __grid_constant__ Maps mp
         // w < 4 takes S columns [0, BN/2), warp w+4 takes [BN/2, BN). The two
         // halves of a row exchange their maxima through shared memory per tile.
         const int grow = row0 + r;
-        const int t = grow < a.M ? grow / a.n_head : a.n_tok - 1;
+        const int t = (grow < a.M ? grow / a.n_head : a.n_tok - 1) - mask_t0;   // row of the mask window
         const int c_base = half * HB;
         for (int i = 0; i < n_my; ++i) {
             wait(bar(C::B_SFULL + (i & 1)), (i >> 1) & 1);
@@ -717,32 +723,44 @@ attn_tc_kernel(const __grid_constant__ TcArgs a, const __grid_constant__ Maps mp
     }
 }
 
-// Merge of the split states written in merge-kernel mode. One CTA per (row,
-// 128-column chunk) of nw = min(kMergeWarps, splits) warps; warp w takes
-// splits w, w + nw, ... (at most a handful each, so the loads of the whole CTA
-// are in flight together). Each warp weighs its splits by 2^(m_s - m_w) against its own
-// maximum m_w; the warp sums are then combined in warp order against the row
-// maximum. The order of every sum is fixed: the result does not depend on
-// timing.
+// Merge of the split states written in merge-kernel mode. A unit is one (row,
+// 128-column chunk); it gets nw warps (one per split when that fits the GPU in
+// one wave, else one per 8 splits, see launch_merge) and a CTA of up to
+// kMergeWarps warps holds several units. Warp w of a unit takes splits
+// w, w + nw, ... (at most a handful each, so the loads of the whole CTA are in
+// flight together). Each warp weighs its splits by 2^(m_s - m_w) against its
+// own maximum m_w; the unit's warp sums are then combined in warp order
+// against the row maximum. The order of every sum is fixed: the result does
+// not depend on timing.
 constexpr int kMergeWarps = 32;
+constexpr int kMergeSplitsPerWarp = 8;          // nw = ceil(splits / 8) warps per unit
 
 template <int HD>
 __global__ void __launch_bounds__(kMergeWarps * 32)
 attn_merge_kernel(const float* __restrict__ part_o, const float2* __restrict__ part_ml, float* __restrict__ out,
-                  int M, int splits) {
+                  int M, int splits, int nw, int early) {
     constexpr int CWM = HD < 128 ? HD : 128;
     constexpr int NCH = HD / CWM;
     constexpr int LANES = CWM / 4;
-    constexpr int PER_WARP = (kMaxMergeSplits + kMergeWarps - 1) / kMergeWarps;
+    constexpr int PER_WARP = kMergeSplitsPerWarp;
     static_assert(PER_WARP <= 32, "one (m, l) pair per lane");
+    static_assert((kMaxMergeSplits + kMergeSplitsPerWarp - 1) / kMergeSplitsPerWarp <= kMergeWarps,
+                  "every split count fits in one CTA");
     __shared__ float s_acc[kMergeWarps][CWM];
     __shared__ float s_m[kMergeWarps], s_l[kMergeWarps];
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, nw = (int)(blockDim.x >> 5);
-    const int row = blockIdx.x / NCH, chunk = blockIdx.x - row * NCH;
+    const int tid = threadIdx.x, lane = tid & 31;
+    const int uw = (tid >> 5) / nw, warp = (tid >> 5) - uw * nw;      // unit in the CTA, warp in the unit
+    const int upc = (int)(blockDim.x >> 5) / nw;                        // units per CTA
+    const int unit = blockIdx.x * upc + uw;
+    const bool live = uw < upc && unit < M * NCH;
+    const int row = live ? unit / NCH : 0, chunk = live ? unit - (unit / NCH) * NCH : 0;
     const int rt = row >> 7, rr = row & 127;
     asm volatile("griddepcontrol.wait;" ::: "memory");     // the attention grid is complete
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    const int n_w = splits > warp ? (splits - warp + nw - 1) / nw : 0;   // this warp's splits
+    // A dependent launch (the next call's qkv_post) may start now only when this
+    // grid fits in one wave; otherwise its waiting CTAs would hold the SMs the
+    // later merge CTAs need.
+    if (early) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    const int n_w = live && splits > warp ? (splits - warp + nw - 1) / nw : 0;   // this warp's splits
     const float2* ml = part_ml + (int64_t)rt * splits * kRows + rr;
     const float2 my_ml =
         lane < n_w ? __ldcg(ml + (int64_t)(warp + nw * lane) * kRows) : make_float2(-INFINITY, 0.f);
@@ -771,25 +789,83 @@ attn_merge_kernel(const float* __restrict__ part_o, const float2* __restrict__ p
         acc.z = fmaf(w, v[u].z, acc.z);
         acc.w = fmaf(w, v[u].w, acc.w);
     }
-    if (lane < LANES) *reinterpret_cast<float4*>(&s_acc[warp][lane * 4]) = acc;
+    const int sw = tid >> 5;                                            // warp slot in the CTA
+    if (lane < LANES) *reinterpret_cast<float4*>(&s_acc[sw][lane * 4]) = acc;
     if (lane == 0) {
-        s_m[warp] = mw;
-        s_l[warp] = lw;
+        s_m[sw] = mw;
+        s_l[sw] = lw;
     }
     __syncthreads();
-    if (row < M) {
+    if (live) {
+        const int w0 = uw * nw;                                         // the unit's first warp slot
         float mx = -INFINITY;
-        for (int w = 0; w < nw; ++w) mx = fmaxf(mx, s_m[w]);
+        for (int w = 0; w < nw; ++w) mx = fmaxf(mx, s_m[w0 + w]);
         const float mref = mx == -INFINITY ? 0.f : mx;
-        for (int c = tid; c < CWM; c += blockDim.x) {      // fewer threads than columns when nw < 4
+        for (int c = warp * 32 + lane; c < CWM; c += nw * 32) {   // fewer threads than columns when nw < 4
             float sum = 0.f, L = 0.f;
 #pragma unroll 4
             for (int w = 0; w < nw; ++w) {
-                const float sc = s_m[w] == -INFINITY ? 0.f : ex2(s_m[w] - mref);
-                sum = fmaf(sc, s_acc[w][c], sum);
-                L = fmaf(sc, s_l[w], L);
+                const float sc = s_m[w0 + w] == -INFINITY ? 0.f : ex2(s_m[w0 + w] - mref);
+                sum = fmaf(sc, s_acc[w0 + w][c], sum);
+                L = fmaf(sc, s_l[w0 + w], L);
             }
             out[(int64_t)row * HD + chunk * CWM + c] = L > 0.f ? sum / L : 0.f;
+        }
+    }
+}
+
+// The same merge for a few splits (<= kSmallMergeSplits): one warp per unit,
+// each lane merging its 4 columns over all splits in registers, units strided
+// over a one-wave grid. Same weights, same order of every sum.
+constexpr int kSmallMergeSplits = 8;
+
+template <int HD>
+__global__ void __launch_bounds__(256)
+attn_merge_small_kernel(const float* __restrict__ part_o, const float2* __restrict__ part_ml,
+                        float* __restrict__ out, int M, int splits) {
+    constexpr int CWM = HD < 128 ? HD : 128;
+    constexpr int NCH = HD / CWM;
+    constexpr int LANES = CWM / 4;
+    asm volatile("griddepcontrol.wait;" ::: "memory");     // the attention grid is complete
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    const int lane = threadIdx.x & 31;
+    const int64_t sstride = (int64_t)kRows * HD;
+    for (int64_t unit = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; unit < (int64_t)M * NCH;
+         unit += ((int64_t)gridDim.x * blockDim.x) >> 5) {
+        const int row = (int)(unit / NCH), chunk = (int)(unit - (int64_t)row * NCH);
+        const int rt = row >> 7, rr = row & 127;
+        const float2* ml = part_ml + (int64_t)rt * splits * kRows + rr;
+        const float* base = part_o + ((int64_t)rt * splits * kRows + rr) * HD + chunk * CWM + (lane % LANES) * 4;
+        float2 st[kSmallMergeSplits];
+        float4 v[kSmallMergeSplits];
+#pragma unroll
+        for (int s2 = 0; s2 < kSmallMergeSplits; ++s2) {
+            st[s2] = s2 < splits ? __ldcg(ml + (int64_t)s2 * kRows) : make_float2(-INFINITY, 0.f);
+            v[s2] = (s2 < splits && lane < LANES) ? __ldcg(reinterpret_cast<const float4*>(base + s2 * sstride))
+                                                 : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+        float mx = -INFINITY;
+#pragma unroll
+        for (int s2 = 0; s2 < kSmallMergeSplits; ++s2) mx = fmaxf(mx, st[s2].x);
+        const float ref = mx == -INFINITY ? 0.f : mx;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        float L = 0.f;
+#pragma unroll
+        for (int s2 = 0; s2 < kSmallMergeSplits; ++s2) {
+            const float w = st[s2].x == -INFINITY ? 0.f : ex2(st[s2].x - ref);
+            L = fmaf(w, st[s2].y, L);
+            acc.x = fmaf(w, v[s2].x, acc.x);
+            acc.y = fmaf(w, v[s2].y, acc.y);
+            acc.z = fmaf(w, v[s2].z, acc.z);
+            acc.w = fmaf(w, v[s2].w, acc.w);
+        }
+        if (lane < LANES) {
+            float4 o;
+            o.x = L > 0.f ? acc.x / L : 0.f;
+            o.y = L > 0.f ? acc.y / L : 0.f;
+            o.z = L > 0.f ? acc.z / L : 0.f;
+            o.w = L > 0.f ? acc.w / L : 0.f;
+            *reinterpret_cast<float4*>(out + (int64_t)row * HD + chunk * CWM + lane * 4) = o;
         }
     }
 }
@@ -799,9 +875,51 @@ fr_status launch_merge(const float* part_o, const float2* part_ml, float* out, i
     if (splits < 1 || splits > kMaxMergeSplits) return FR_ERR_UNSUPPORTED;
     cudaLaunchConfig_t cfg;
     memset(&cfg, 0, sizeof(cfg));
+    if (splits <= kSmallMergeSplits) {
+        int dev = 0, sms = 152;
+        if (cudaGetDevice(&dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return FR_ERR_CUDA;
+        const int64_t units = (int64_t)M * (hd < 128 ? 1 : hd / 128);
+        const int64_t want = (units + 7) / 8;                       // 8 warps (units) per CTA
+        cfg.gridDim = dim3((unsigned)(want < (int64_t)sms * 8 ? want : (int64_t)sms * 8), 1, 1);
+        cfg.blockDim = dim3(256, 1, 1);
+        cfg.stream = stream;
+        cudaLaunchAttribute at[1];
+        at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        at[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = at;
+        cfg.numAttrs = 1;
+        cudaError_t e;
+        switch (hd) {
+            case 64: e = cudaLaunchKernelEx(&cfg, attn_merge_small_kernel<64>, part_o, part_ml, out, M, splits); break;
+            case 128: e = cudaLaunchKernelEx(&cfg, attn_merge_small_kernel<128>, part_o, part_ml, out, M, splits); break;
+            default: e = cudaLaunchKernelEx(&cfg, attn_merge_small_kernel<256>, part_o, part_ml, out, M, splits); break;
+        }
+        return e == cudaSuccess ? FR_OK : FR_ERR_CUDA;
+    }
     const int nch = hd < 128 ? 1 : hd / 128;
-    cfg.gridDim = dim3(M * nch, 1, 1);
-    cfg.blockDim = dim3((splits < kMergeWarps ? splits : kMergeWarps) * 32, 1, 1);
+    const int units = M * nch;
+    int dev = 0, sms = 152;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return FR_ERR_CUDA;
+    // Warps per unit and units per CTA. When one warp per split fits the GPU in
+    // one wave, take that (the fewest dependent loads per warp). Otherwise up to
+    // 8 splits per warp (fewer instructions per split), with few enough units
+    // per CTA that the grid still covers the SMs.
+    int nw, upc;
+    if ((int64_t)units * splits <= (int64_t)sms * kMergeWarps && splits <= kMergeWarps) {
+        nw = splits;
+        upc = kMergeWarps / nw;
+    } else {
+        nw = (splits + kMergeSplitsPerWarp - 1) / kMergeSplitsPerWarp;
+        upc = kMergeWarps / nw;
+        if (upc > units / sms) upc = units / sms > 0 ? units / sms : 1;
+    }
+    cfg.gridDim = dim3((units + upc - 1) / upc, 1, 1);
+    cfg.blockDim = dim3(upc * nw * 32, 1, 1);
+    const int early = (int64_t)cfg.gridDim.x * cfg.blockDim.x <= (int64_t)sms * 2048 ? 1 : 0;   // one wave
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -810,9 +928,9 @@ fr_status launch_merge(const float* part_o, const float2* part_ml, float* out, i
     cfg.numAttrs = 1;
     cudaError_t e;
     switch (hd) {
-        case 64: e = cudaLaunchKernelEx(&cfg, attn_merge_kernel<64>, part_o, part_ml, out, M, splits); break;
-        case 128: e = cudaLaunchKernelEx(&cfg, attn_merge_kernel<128>, part_o, part_ml, out, M, splits); break;
-        default: e = cudaLaunchKernelEx(&cfg, attn_merge_kernel<256>, part_o, part_ml, out, M, splits); break;
+        case 64: e = cudaLaunchKernelEx(&cfg, attn_merge_kernel<64>, part_o, part_ml, out, M, splits, nw, early); break;
+        case 128: e = cudaLaunchKernelEx(&cfg, attn_merge_kernel<128>, part_o, part_ml, out, M, splits, nw, early); break;
+        default: e = cudaLaunchKernelEx(&cfg, attn_merge_kernel<256>, part_o, part_ml, out, M, splits, nw, early); break;
     }
     return e == cudaSuccess ? FR_OK : FR_ERR_CUDA;
 }
@@ -881,7 +999,9 @@ static fr_status launch(const TcLaunch& L, cudaStream_t stream) {
     constexpr int BN = Cfg<HD>::BN;
     if (!encode_2d(&mp.k, L.k, HD, a.n_kv, L.k_rs, 64, BN)) return FR_ERR_CUDA;
     if (!encode_2d(&mp.v, L.v, HD, a.n_kv, L.v_rs, 64, BN)) return FR_ERR_CUDA;
-    if (a.has_mask && !encode_2d(&mp.mask, L.mask, a.n_kv, a.n_tok, L.m_rs, 64, a.n_tok)) return FR_ERR_CUDA;
+    if (a.has_mask &&
+        !encode_2d(&mp.mask, L.mask, a.n_kv, a.n_tok, L.m_rs, 64, (uint32_t)(a.n_tok < kMaskWin ? a.n_tok : kMaskWin)))
+        return FR_ERR_CUDA;
     if (!a.q16 || !encode_2d(&mp.q16, a.q16, HD, a.M, HD, 64, kRows / a.C)) return FR_ERR_CUDA;
     if (a.merge_kernel &&
         !encode_2d_f32(&mp.po, a.part_o, HD, (uint64_t)L.row_tiles * a.splits * kRows, kOutBoxRows))

@@ -13,8 +13,21 @@
 namespace fr {
 
 constexpr int kMaxPairs = 128;     // hd 256 -> 128 rotated pairs at most
-constexpr int kMaxTok = 16;        // q_tokens <= 16
-constexpr int kMaxRows = 512;      // M = n_tok * n_head
+constexpr int kMaxTok = 16;        // q_tokens <= 16 (decode; the mma.sync engine's bound)
+constexpr int kMaxRows = 512;      // M = n_tok * n_head (decode)
+// The tcgen05 engine also takes longer query windows (prefill): each 128-row
+// tile reads a window of kMaskWin consecutive tokens' mask rows, which holds
+// every token of the tile when n_tok <= kMaskWin or n_head >= 8.
+constexpr int kMaxTokTc = 8192;
+constexpr int kMaxRowsTc = 65536;
+constexpr int kMaskWin = 16;
+inline bool tc_shape_ok(int n_tok, int n_head) {
+    return n_tok >= 1 && n_head >= 1 && n_tok <= kMaxTokTc && (int64_t)n_tok * n_head <= kMaxRowsTc &&
+           (n_tok <= kMaskWin || n_head >= 8);
+}
+inline bool decode_shape(int n_tok, int n_head) {
+    return n_tok >= 1 && n_head >= 1 && n_tok <= kMaxTok && (int64_t)n_tok * n_head <= kMaxRows;
+}
 
 // Per-launch RoPE constants (kernel parameter, by value).
 //   turns[i] = frac(w_i / 2pi) * 2^64, w_i = effective angle per position of

@@ -386,9 +386,13 @@ static size_t v1_workspace_bytes(int M, int hd, int n_kv) {
 // [cluster partial O][cluster partial (m, l)].
 static size_t tc_q16_bytes(int M, int hd) { return ((size_t)M * hd * 2 + 1023) & ~(size_t)1023; }
 
+// Up to kMaxClusters clusters per row tile for at most kMaxRowTilesMulti row
+// tiles; more row tiles fill the GPU alone and get one cluster each.
+constexpr int kMaxRowTilesMulti = 4;
+
 static size_t tc_workspace_bytes(int M, int hd) {
     const size_t row_tiles = (size_t)(M + 127) / 128;
-    const size_t slots = row_tiles * tc::kMaxClusters * 128;
+    const size_t slots = row_tiles * (row_tiles <= (size_t)kMaxRowTilesMulti ? tc::kMaxClusters : 1) * 128;
     return kWsHeader + tc_q16_bytes(M, hd) + slots * hd * sizeof(float) + slots * sizeof(float2);
 }
 
@@ -402,9 +406,13 @@ static size_t tc_merge_workspace_bytes(int M, int hd) {
     return tc_merge_fixed_bytes(M, hd) + (size_t)tc_merge_max_splits(M) * tc_merge_split_bytes(M, hd);
 }
 
-// Smallest workspace any plan of this shape accepts (in-kernel merge).
-static size_t workspace_bytes_for(int M, int hd, int n_kv) {
-    const size_t a = v1_workspace_bytes(M, hd, n_kv), b = tc_workspace_bytes(M, hd);
+// Smallest workspace any plan of this shape accepts (in-kernel merge); the
+// mma.sync engine's needs count only for the shapes it takes.
+static size_t workspace_bytes_for(int n_tok, int n_head, int hd, int n_kv) {
+    const int M = n_tok * n_head;
+    const size_t b = tc_workspace_bytes(M, hd);
+    if (!decode_shape(n_tok, n_head)) return b;
+    const size_t a = v1_workspace_bytes(M, hd, n_kv);
     return a > b ? a : b;
 }
 
@@ -437,6 +445,7 @@ static TcPlan make_tc_plan(int M, int hd, int n_kv, int num_sms, int force_split
         n_cl = min(n_cl, (p.n_tiles + 2 * C - 1) / (2 * C));
     }
     n_cl = max(1, min(n_cl, min(tc::kMaxClusters, (p.n_tiles + C - 1) / C)));
+    if (p.row_tiles > kMaxRowTilesMulti) n_cl = 1;   // many row tiles fill the GPU without more splits
     int S = C * n_cl;
     p.tiles_per_split = (p.n_tiles + S - 1) / S;
     // drop clusters that would get no tile at all
@@ -465,6 +474,10 @@ static TcPlan choose_tc_plan(int M, int hd, int n_kv, int num_sms, const fr_attn
     else use = p.splits > 2;
     if (!use) return p;
     const int cap = tc_merge_max_splits(M);
+    if (cap < 1) {                                    // more row tiles than split slots
+        if (o.merge_mode == 2) *ok = false;
+        return p;
+    }
     int S = o.force_splits > 0 ? o.force_splits : max(1, num_sms / p.row_tiles);
     S = max(1, min(S, min(cap, p.n_tiles)));
     const size_t fixed = tc_merge_fixed_bytes(M, hd);
@@ -522,7 +535,8 @@ static fr_status decode_attn_impl(const uint16_t* q16, const float* q, int64_t q
     if (!k || !v || !out || !ws) return FR_ERR_INVALID_ARG;
     if (n_tok < 1 || n_head < 1 || n_kv < 1) return FR_ERR_INVALID_ARG;
     if (hd != 64 && hd != 128 && hd != 256) return FR_ERR_UNSUPPORTED;
-    if (n_tok > kMaxTok || (int64_t)n_tok * n_head > kMaxRows) return FR_ERR_UNSUPPORTED;
+    if (!tc_shape_ok(n_tok, n_head)) return FR_ERR_UNSUPPORTED;
+    if (o.engine == 1 && !decode_shape(n_tok, n_head)) return FR_ERR_UNSUPPORTED;
     if (n_kv > (1 << 26)) return FR_ERR_UNSUPPORTED;
     if (!isfinite(kq_scale)) return FR_ERR_INVALID_ARG;
     if (k_rs < hd || (k_rs & 7) || v_rs < hd || (v_rs & 7)) return FR_ERR_INVALID_ARG;
@@ -539,7 +553,7 @@ static fr_status decode_attn_impl(const uint16_t* q16, const float* q, int64_t q
         if (!build_rope_table(rp, q_scale, hd, &tb)) return FR_ERR_INVALID_ARG;
     }
     const int M = n_tok * n_head;
-    if (ws_bytes < workspace_bytes_for(M, hd, n_kv)) return FR_ERR_WORKSPACE;
+    if (ws_bytes < workspace_bytes_for(n_tok, n_head, hd, n_kv)) return FR_ERR_WORKSPACE;
 
     int dev = 0, sms = 152;
     if (cudaGetDevice(&dev) != cudaSuccess) return FR_ERR_CUDA;
@@ -581,6 +595,10 @@ static fr_status decode_attn_impl(const uint16_t* q16, const float* q, int64_t q
         a.n_clusters = p.n_clusters;
         a.C = p.C;
         a.merge_kernel = p.merge_kernel;
+        {   // one wave: at one CTA per SM, the co-resident CTAs for this cluster size
+            const int cap = p.C >= 8 ? (sms * 120) / 152 : (p.C == 4 ? (sms * 144) / 152 : sms);
+            a.early_dep = p.row_tiles * p.splits <= cap ? 1 : 0;
+        }
         a.splits = p.splits;
         a.kq_log2 = kq_scale * kLog2e;
         a.wait_limit_ns = tc::kWaitLimitNs;
@@ -635,12 +653,12 @@ static fr_status decode_attn_impl(const uint16_t* q16, const float* q, int64_t q
 using namespace fr;
 
 extern "C" size_t fr_decode_attn_workspace_size(int n_tok, int n_head, int hd, int n_kv) {
-    if (n_tok < 1 || n_tok > kMaxTok || n_head < 1 || (int64_t)n_tok * n_head > kMaxRows) return 0;
+    if (!tc_shape_ok(n_tok, n_head)) return 0;
     if ((hd != 64 && hd != 128 && hd != 256) || n_kv < 1 || n_kv > (1 << 26)) return 0;
     const int M = n_tok * n_head;
     // room for every plan, the merge-kernel one included
-    const size_t base = workspace_bytes_for(M, hd, n_kv);
-    const size_t merge = tc_merge_workspace_bytes(M, hd);
+    const size_t base = workspace_bytes_for(n_tok, n_head, hd, n_kv);
+    const size_t merge = tc_merge_max_splits(M) >= 1 ? tc_merge_workspace_bytes(M, hd) : 0;
     return merge > base ? merge : base;
 }
 
@@ -657,7 +675,8 @@ extern "C" fr_status fr_decode_attn_plan(int n_tok, int n_head, int hd, int n_kv
         o.force_cluster != 8)
         return FR_ERR_INVALID_ARG;
     const int M = n_tok * n_head;
-    if (workspace_bytes < workspace_bytes_for(M, hd, n_kv)) return FR_ERR_WORKSPACE;
+    if (o.engine == 1 && !decode_shape(n_tok, n_head)) return FR_ERR_UNSUPPORTED;
+    if (workspace_bytes < workspace_bytes_for(n_tok, n_head, hd, n_kv)) return FR_ERR_WORKSPACE;
     int dev = 0, sms = 152;
     if (cudaGetDevice(&dev) != cudaSuccess) return FR_ERR_CUDA;
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return FR_ERR_CUDA;
@@ -685,7 +704,7 @@ extern "C" fr_status fr_decode_attn_plan(int n_tok, int n_head, int hd, int n_kv
 namespace fr {
 size_t decode_attn_min_workspace_bytes(int n_tok, int n_head, int hd, int n_kv) {
     if (fr_decode_attn_workspace_size(n_tok, n_head, hd, n_kv) == 0) return 0;
-    return workspace_bytes_for(n_tok * n_head, hd, n_kv);
+    return workspace_bytes_for(n_tok, n_head, hd, n_kv);
 }
 }  // namespace fr
 

@@ -67,8 +67,9 @@ bool build_rope_table(const fr_rope_params* rp, float q_scale, int hd, RopeTable
     return true;
 }
 
-// One thread per slot (hd/2 slots per row); blockDim.x = hd/2 rows-slots,
-// blockDim.y rows per block.
+// One thread per slot (hd/2 slots per row); blockDim.x = hd/2 slots,
+// blockDim.y rows per block, rows strided over the grid (at most one wave of
+// CTAs, so a dependent launch is released as soon as every CTA has started).
 template <int HD>
 __global__ void __launch_bounds__(256)
 qkv_post_kernel(const float* __restrict__ q, int64_t q_tok_stride, const int32_t* __restrict__ pos,
@@ -80,23 +81,38 @@ qkv_post_kernel(const float* __restrict__ q, int64_t q_tok_stride, const int32_t
     // waits for this grid's completion before it reads the rows.
     asm volatile("griddepcontrol.wait;" ::: "memory");
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    const int r = blockIdx.x * blockDim.y + threadIdx.y;
-    if (r >= M) return;
     const int c = threadIdx.x;                 // slot 0 .. HD/2-1
-    const int t = r / n_head, h = r - t * n_head;
-    const float* qrow = q + (int64_t)t * q_tok_stride + (int64_t)h * HD;
-    int d0, d1;
-    float y0, y1;
-    rope_slot(qrow, c, __ldg(pos + t), tb, d0, d1, y0, y1);
-    __half* orow = q16 + (int64_t)r * HD;
-    orow[d0] = __float2half_rn(y0);
-    orow[d1] = __float2half_rn(y1);
-    if (q32) {
-        float* frow = q32 + (int64_t)r * HD;
-        frow[d0] = y0;
-        frow[d1] = y1;
+    // the table in shared memory: indexing the parameter copy with a
+    // per-thread slot would serialise every access
+    __shared__ RopeTable stb;
+    if (threadIdx.y == 0) {
+        stb.turns[c] = tb.turns[c];
+        if (c == 0) {
+            stb.mscale = tb.mscale;
+            stb.q_scale = tb.q_scale;
+            stb.half = tb.half;
+            stb.n_dims = tb.n_dims;
+        }
+    }
+    __syncthreads();
+    for (int r = blockIdx.x * blockDim.y + threadIdx.y; r < M; r += gridDim.x * blockDim.y) {
+        const int t = r / n_head, h = r - t * n_head;
+        const float* qrow = q + (int64_t)t * q_tok_stride + (int64_t)h * HD;
+        int d0, d1;
+        float y0, y1;
+        rope_slot(qrow, c, __ldg(pos + t), stb, d0, d1, y0, y1);
+        __half* orow = q16 + (int64_t)r * HD;
+        orow[d0] = __float2half_rn(y0);
+        orow[d1] = __float2half_rn(y1);
+        if (q32) {
+            float* frow = q32 + (int64_t)r * HD;
+            frow[d0] = y0;
+            frow[d1] = y1;
+        }
     }
 }
+
+constexpr int kQkvMaxCtas = 1216;            // 8 CTAs of 256 threads on each of 152 SMs
 
 fr_status launch_qkv_post(const float* q, int64_t q_tok_stride, const int32_t* pos, int n_tok, int n_head,
                           int hd, const RopeTable& tb, uint16_t* q16_out, float* q32_out, cudaStream_t stream) {
@@ -104,7 +120,7 @@ fr_status launch_qkv_post(const float* q, int64_t q_tok_stride, const int32_t* p
     const int slots = hd / 2;
     const int rows_per_block = 256 / slots;
     dim3 block(slots, rows_per_block);
-    dim3 grid((M + rows_per_block - 1) / rows_per_block);
+    dim3 grid(min((M + rows_per_block - 1) / rows_per_block, kQkvMaxCtas));
     __half* o16 = reinterpret_cast<__half*>(q16_out);
     // programmatic dependent launch: this grid may be scheduled while the
     // previous one on the stream finishes (the kernel waits before any access)
@@ -139,6 +155,15 @@ kv_append_kernel(const float* __restrict__ k_new, int64_t k_stride, const float*
                  const __grid_constant__ RopeTable tb) {
     asm volatile("griddepcontrol.wait;" ::: "memory");
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    __shared__ RopeTable stb;                                  // see qkv_post_kernel
+    for (int i = threadIdx.x; i < kMaxPairs; i += blockDim.x) stb.turns[i] = tb.turns[i];
+    if (threadIdx.x == 0) {
+        stb.mscale = tb.mscale;
+        stb.q_scale = tb.q_scale;
+        stb.half = tb.half;
+        stb.n_dims = tb.n_dims;
+    }
+    __syncthreads();
     constexpr int G = HD / 8;                                  // 8-element groups per row
     const int64_t nK = (int64_t)n_tok * (HD / 2), nV = (int64_t)n_tok * G, nP = pad_rows * G;
     for (int64_t w = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; w < nK + nV + nP;
@@ -147,7 +172,7 @@ kv_append_kernel(const float* __restrict__ k_new, int64_t k_stride, const float*
             const int t = (int)(w / (HD / 2)), c = (int)(w - (int64_t)t * (HD / 2));
             int d0, d1;
             float y0, y1;
-            rope_slot(k_new + (int64_t)t * k_stride, c, __ldg(pos + t), tb, d0, d1, y0, y1);
+            rope_slot(k_new + (int64_t)t * k_stride, c, __ldg(pos + t), stb, d0, d1, y0, y1);
             __half* krow = k_cache + (row0 + t) * k_rs;
             krow[d0] = __float2half_rn(y0);
             krow[d1] = __float2half_rn(y1);
@@ -194,7 +219,7 @@ extern "C" fr_status fr_kv_append(const float* k_new, int64_t k_stride, const fl
     if (!k_new || !v_new || !pos || !rp || !k_cache || !v_cache) return FR_ERR_INVALID_ARG;
     if (n_tok < 1 || hd < 1) return FR_ERR_INVALID_ARG;
     if (hd != 64 && hd != 128 && hd != 256) return FR_ERR_UNSUPPORTED;
-    if (n_tok > kMaxTok) return FR_ERR_UNSUPPORTED;
+    if (n_tok > kMaxTokTc) return FR_ERR_UNSUPPORTED;
     if (k_stride < hd || (k_stride & 3) || v_stride < hd || (v_stride & 3)) return FR_ERR_INVALID_ARG;
     if (k_row_stride < hd || (k_row_stride & 7) || v_row_stride < hd || (v_row_stride & 7))
         return FR_ERR_INVALID_ARG;
@@ -254,7 +279,7 @@ extern "C" fr_status fr_qkv_post(const float* q, int64_t q_tok_stride, const int
     if (!q || !pos || !rp || !q16_out) return FR_ERR_INVALID_ARG;
     if (n_tok < 1 || n_head < 1 || hd < 1) return FR_ERR_INVALID_ARG;
     if (hd != 64 && hd != 128 && hd != 256) return FR_ERR_UNSUPPORTED;
-    if (n_tok > kMaxTok || (int64_t)n_tok * n_head > kMaxRows) return FR_ERR_UNSUPPORTED;
+    if (n_tok > kMaxTokTc || (int64_t)n_tok * n_head > kMaxRowsTc) return FR_ERR_UNSUPPORTED;
     if (q_tok_stride < (int64_t)n_head * hd || (q_tok_stride & 3)) return FR_ERR_INVALID_ARG;
     if (!aligned16(q) || !aligned16(q16_out) || (q32_out && !aligned16(q32_out)))
         return FR_ERR_INVALID_ARG;

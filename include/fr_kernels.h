@@ -98,7 +98,7 @@ int fr_abi_version(void);
  *
  * Arithmetic: angles reduced exactly modulo one turn (64-bit fixed point),
  * rotation and scale in fp32, one round-to-nearest to f16.
- * Supported: 1 <= n_tok <= 16, 1 <= n_head, M = n_tok*n_head <= 512,
+ * Supported: 1 <= n_tok <= 8192, 1 <= n_head, M = n_tok*n_head <= 65536,
  * hd in {64, 128, 256}.
  */
 fr_status fr_qkv_post(const float* q, int64_t q_tok_stride, const int32_t* pos,
@@ -132,7 +132,7 @@ fr_status fr_qkv_post(const float* q, int64_t q_tok_stride, const int32_t* pos,
  * before reading. A following fr_decode_attn on the same stream sees the new
  * rows: its qkv_post kernel waits for this grid before it releases the
  * attention launch.
- * Supported: 1 <= n_tok <= 16, hd in {64, 128, 256}.
+ * Supported: 1 <= n_tok <= 8192, hd in {64, 128, 256}.
  */
 fr_status fr_kv_append(const float* k_new, int64_t k_stride, const float* v_new, int64_t v_stride,
                        const int32_t* pos, int n_tok, int hd, const fr_rope_params* rp,
@@ -184,7 +184,12 @@ fr_status fr_workspace_check(void* workspace, cudaStream_t stream);
  *   workspace, workspace_bytes: >= fr_decode_attn_workspace_size(...), zeroed
  *            once; one workspace per concurrently running call.
  *
- * Supported: 1 <= n_tok <= 16, M <= 512, hd in {64, 128, 256}, n_kv >= 1.
+ * Supported: hd in {64, 128, 256}, n_kv >= 1, and
+ *   decode windows: 1 <= n_tok <= 16, M <= 512 (both engines);
+ *   longer query windows (prefill, e.g. a prefix with KV length = query
+ *   count and a pad-only mask): n_tok <= 8192, M <= 65536, with n_tok <= 16
+ *   or n_head >= 8 (every 128-row tile then spans at most 16 consecutive
+ *   tokens, whose mask rows it reads as one window); tcgen05 engine only.
  */
 fr_status fr_decode_attn(const uint16_t* q16,
                          const float* q, int64_t q_tok_stride, const int32_t* pos,

@@ -50,8 +50,10 @@ def test_status_strings_and_version(lib):
 def test_workspace_size_host_logic(lib):
     ws = lib.fr_decode_attn_workspace_size
     assert ws(10, 8, 256, 1024) > 0
-    assert ws(17, 1, 128, 64) == 0          # q_tokens > 16
-    assert ws(16, 33, 128, 64) == 0         # M > 512
+    assert ws(17, 1, 128, 64) == 0          # > 16 tokens with < 8 heads: no 16-token mask window
+    assert ws(17, 8, 128, 64) > 0           # prefill window, 8 heads
+    assert ws(16, 4097, 128, 64) == 0       # M > 65536
+    assert ws(8193, 8, 128, 64) == 0        # n_tok > 8192
     assert ws(1, 1, 96, 64) == 0            # unsupported hd
     assert ws(1, 1, 128, 0) == 0
     assert ws(16, 8, 128, 65536) >= ws(16, 8, 128, 4096) >= ws(16, 8, 128, 64)
@@ -75,8 +77,8 @@ def _attn(lib, q16=FAKE, k=FAKE, v=FAKE, mask=None, k_rs=128, m_rs=0, n_tok=4, n
 def test_decode_attn_validation(lib):
     assert _attn(lib, k=None) == 1
     assert _attn(lib, hd=96) == 2
-    assert _attn(lib, n_tok=17) == 2
-    assert _attn(lib, n_tok=16, n_head=33) == 2
+    assert _attn(lib, n_tok=17, n_head=4) == 2
+    assert _attn(lib, n_tok=16, n_head=4097) == 2
     assert _attn(lib, n_kv=0) == 1
     assert _attn(lib, k_rs=100) == 1                 # stride not a multiple of 8
     assert _attn(lib, k_rs=64) == 1                  # stride < hd
@@ -103,7 +105,7 @@ def test_qkv_post_validation(lib):
     assert call(q=None) == 1
     assert call(out=None) == 1
     assert call(hd=80) == 2
-    assert call(n_tok=17) == 2
+    assert call(n_tok=8193) == 2
     assert call(stride=8 * 128 - 4) == 1
     assert call(stride=8 * 128 + 2) == 1
     assert call(q=MIS) == 1
@@ -122,7 +124,7 @@ def test_plan_validation(lib):
         n_tok, 8, hd, 1024, 1, ws, opts, out)
     assert call(out=None) == 1
     assert call(hd=96) == 2
-    assert call(n_tok=17) == 2
+    assert call(n_tok=8193) == 2
     assert call(ws=64) == 3
     assert call(opts=ctypes.byref(FrAttnOpts(0, 0, 0, 0, 5))) == 1
     assert call(opts=ctypes.byref(FrAttnOpts(0, 0, 3, 0, 0))) == 1
@@ -137,6 +139,23 @@ def test_workspace_size_covers_the_merge_kernel_plan(lib):
         assert ws(n_tok, n_head, hd, 1024) >= (160 // rt) * rt * 128 * (hd * 4 + 8)
 
 
+def test_prefill_shapes_host_logic(lib):
+    """Longer query windows run on the tcgen05 engine only; the mma.sync
+    engine keeps the decode bounds."""
+    from gqa_kv_head_gb300._abi import FrAttnOpts, FrAttnPlan
+    n_tok, n_head, hd, n_kv = 968, 8, 256, 1024
+    ws = lib.fr_decode_attn_workspace_size(n_tok, n_head, hd, n_kv)
+    assert ws > 0
+    # no per-row-tile cluster partials beyond 4 row tiles: the workspace stays modest
+    assert ws < 64 << 20
+    plan = FrAttnPlan()
+    assert lib.fr_decode_attn_plan(n_tok, n_head, hd, n_kv, 1, ws, ctypes.byref(FrAttnOpts(1, 0, 0, 0, 0)),
+                                   ctypes.byref(plan)) == 2
+    assert lib.fr_decode_attn_ex(FAKE, None, 0, None, None, 0.0, FAKE, hd, FAKE, hd, None, 0,
+                                 n_tok, n_head, hd, n_kv, 1.0, FAKE, FAKE, ws,
+                                 ctypes.byref(FrAttnOpts(1, 0, 0, 0, 0)), None) == 2
+
+
 def test_kv_append_validation(lib):
     rp = _rope(lib)
     def call(k=FAKE, v=FAKE, pos=FAKE, n_tok=4, hd=128, ks=128, kr=128, n_ctx=64, row0=10, pb=40, pe=64,
@@ -146,7 +165,7 @@ def test_kv_append_validation(lib):
     assert call(k=None) == 1
     assert call(pos=None) == 1
     assert call(hd=96) == 2
-    assert call(n_tok=17) == 2
+    assert call(n_tok=8193) == 2
     assert call(ks=100) == 1                 # f32 row stride not a multiple of 4
     assert call(ks=64) == 1                  # stride < hd
     assert call(kr=132) == 1                 # f16 row stride not a multiple of 8
