@@ -68,7 +68,7 @@ constexpr float kTau = 8.0f;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr uint32_t kTmemCols = 512;
 constexpr int kOutBoxRows = 32;              // rows per TMA store box of the split states
-static_assert(kRows % kOutBoxRows == 0 && kOutBoxRows % 8 == 0, "whole 128-byte swizzle periods per box");
+static_assert(kOutBoxRows == 32, "one box block = the 32 rows of one softmax warp");
 
 template <int HD>
 struct Cfg {
@@ -507,47 +507,40 @@ attn_tc_kernel(const __grid_constant__ TcArgs a, const __grid_constant__ Maps mp
     if (a.merge_kernel) {
         // ---- merge-kernel mode: this split's (m, l, O) rows go to the workspace;
         // attn_merge_kernel merges them. O leaves TMEM into the stage area (free
-        // now) as HD/32 boxes of [128 rows][32 fp32] in the 128-byte swizzle, and
-        // goes out as TMA tensor stores.
-        if (warp < kSmaxWarps) {
+        // now) as HD/32 boxes of [128 rows][32 fp32] in the 128-byte swizzle.
+        // Each softmax warp fills the [32 rows][32 fp32] block of one box per
+        // TMEM chunk and stores it by TMA at once, so the stores of the first
+        // chunks overlap the TMEM reads of the later ones. Warps whose 32 rows
+        // hold no real row store nothing.
+        if (warp < kSmaxWarps && quad_active) {
             unsigned char* sOut = sStage;
-            if (quad_active) {
-                tc_fence_after();
+            const int y = (rt * a.splits + split) * kRows + qd * 32;
+            tc_fence_after();
 #pragma unroll 1
-                for (int c = 0; c < OH; c += 32) {
-                    uint32_t o[32];
-                    if (n_my > 0) {
-                        tmem_ld_x32(tbase + lane_base + C::TM_O + half * OH + c, o);
-                        tmem_wait_ld();
-                    } else {
+            for (int c = 0; c < OH; c += 32) {
+                uint32_t o[32];
+                if (n_my > 0) {
+                    tmem_ld_x32(tbase + lane_base + C::TM_O + half * OH + c, o);
+                    tmem_wait_ld();
+                } else {
 #pragma unroll
-                        for (int u = 0; u < 32; ++u) o[u] = 0u;
-                    }
-                    unsigned char* rowp = sOut + ((half * OH + c) >> 5) * C::OBOX + r * 128;
-#pragma unroll
-                    for (int j = 0; j < 8; ++j)
-                        *reinterpret_cast<uint4*>(rowp + ((j ^ (r & 7)) << 4)) =
-                            make_uint4(o[4 * j], o[4 * j + 1], o[4 * j + 2], o[4 * j + 3]);
+                    for (int u = 0; u < 32; ++u) o[u] = 0u;
                 }
-                if (half == 0 && r < rows_real)
-                    a.part_ml[(int64_t)(rt * a.splits + split) * kRows + r] =
-                        n_my > 0 ? make_float2(m_ref, l_part) : make_float2(-INFINITY, 0.f);
+                const int bx = (half * OH + c) >> 5;
+                unsigned char* rowp = sOut + bx * C::OBOX + r * 128;
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    *reinterpret_cast<uint4*>(rowp + ((j ^ (r & 7)) << 4)) =
+                        make_uint4(o[4 * j], o[4 * j + 1], o[4 * j + 2], o[4 * j + 3]);
+                fence_proxy_async_cta();        // the block is read by the TMA engine
+                __syncwarp();
+                if (lane == 0) tma_store_2d(&mp.po, bx * 32, y, smem_addr(sOut + bx * C::OBOX + qd * 32 * 128));
             }
-            fence_proxy_async_cta();        // the boxes are read by the TMA engine
-            softmax_bar_sync();
-            if (warp == 0 && lane == 0) {
-                // only the 32-row blocks that hold real rows
-                const int y = (rt * a.splits + split) * kRows;
-                const int n_rb = (rows_real + kOutBoxRows - 1) / kOutBoxRows;
-#pragma unroll 1
-                for (int rb = 0; rb < n_rb; ++rb)
-#pragma unroll 1
-                    for (int bx = 0; bx < HD / 32; ++bx)
-                        tma_store_2d(&mp.po, bx * 32, y + rb * kOutBoxRows,
-                                     smem_addr(sOut + bx * C::OBOX + rb * kOutBoxRows * 128));
-                bulk_commit();
-                bulk_wait_all();            // performed before the grid completes
-            }
+            if (lane == 0) bulk_commit();
+            if (half == 0 && r < rows_real)
+                a.part_ml[(int64_t)(rt * a.splits + split) * kRows + r] =
+                    n_my > 0 ? make_float2(m_ref, l_part) : make_float2(-INFINITY, 0.f);
+            if (lane == 0) bulk_wait_all();     // performed before the grid completes
         }
     } else {
     // ---- push (m, l, O) rows to the CTA that owns them in this cluster ------
