@@ -76,7 +76,7 @@ struct Cfg {
     // Separate rings for K, V and mask tiles: a K slot frees when S_j is
     // computed, a V slot when PV_j is, a mask slot when the softmax has read
     // it, so K tiles run ahead of the V tiles they travel with.
-    static constexpr int KS = HD == 256 ? 2 : (HD == 128 ? 5 : 8);   // K slots
+    static constexpr int KS = HD == 256 ? 2 : (HD == 128 ? 3 : 8);   // K slots
     static constexpr int VS = KS;                                     // V slots
     static constexpr int MS = 4;                                      // mask slots
     static constexpr int NB = HD / 64;                     // 128-byte column boxes per row
