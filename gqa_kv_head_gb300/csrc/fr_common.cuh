@@ -50,6 +50,9 @@ bool build_rope_table(const fr_rope_params* rp, float q_scale, int hd, RopeTable
 // lets a programmatically dependent launch start early.
 fr_status launch_qkv_post(const float* q, int64_t q_tok_stride, const int32_t* pos, int n_tok, int n_head,
                           int hd, const RopeTable& tb, uint16_t* q16_out, float* q32_out, cudaStream_t stream);
+// Threads per qkv_post CTA and query heads per work item (one cos/sin each).
+constexpr int kQkvThreads = 256;
+constexpr int kQkvHeads = 4;
 
 // Scaled cosine and sine of pair i at integer position pos.
 __device__ __forceinline__ void rope_cs(int pos, uint64_t turns, float mscale, float& c, float& s) {
@@ -83,19 +86,31 @@ __device__ __forceinline__ void rope_pair(float x0, float x1, int pos, uint64_t 
 // One "slot" of a Q row: slot c < half rotates dims (c, c + half); slot
 // c >= half passes dims n_dims + 2(c - half) and +1 through (scaled).
 // hd/2 slots cover the row exactly.
-__device__ __forceinline__ void rope_slot(const float* __restrict__ qrow, int c, int pos,
-                                          const RopeTable& tb, int& d0, int& d1,
-                                          float& y0, float& y1) {
+// The two dims of slot c.
+__device__ __forceinline__ void rope_slot_dims(int c, const RopeTable& tb, int& d0, int& d1) {
     if (c < tb.half) {
         d0 = c;
         d1 = c + tb.half;
-        rope_pair(qrow[d0], qrow[d1], pos, tb.turns[c], tb.mscale, tb.q_scale, y0, y1);
     } else {
         d0 = tb.n_dims + 2 * (c - tb.half);
         d1 = d0 + 1;
-        y0 = __fmul_rn(qrow[d0], tb.q_scale);
-        y1 = __fmul_rn(qrow[d1], tb.q_scale);
     }
+}
+// Slot c applied to its two inputs x0 = row[d0], x1 = row[d1].
+__device__ __forceinline__ void rope_slot_apply(int c, float x0, float x1, int pos, const RopeTable& tb,
+                                                float& y0, float& y1) {
+    if (c < tb.half) {
+        rope_pair(x0, x1, pos, tb.turns[c], tb.mscale, tb.q_scale, y0, y1);
+    } else {
+        y0 = __fmul_rn(x0, tb.q_scale);
+        y1 = __fmul_rn(x1, tb.q_scale);
+    }
+}
+__device__ __forceinline__ void rope_slot(const float* __restrict__ qrow, int c, int pos,
+                                          const RopeTable& tb, int& d0, int& d1,
+                                          float& y0, float& y1) {
+    rope_slot_dims(c, tb, d0, d1);
+    rope_slot_apply(c, qrow[d0], qrow[d1], pos, tb, y0, y1);
 }
 
 inline bool aligned16(const void* p) { return (((uintptr_t)p) & 15u) == 0; }

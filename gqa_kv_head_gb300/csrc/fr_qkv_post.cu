@@ -67,13 +67,14 @@ bool build_rope_table(const fr_rope_params* rp, float q_scale, int hd, RopeTable
     return true;
 }
 
-// One thread per slot (hd/2 slots per row); blockDim.x = hd/2 slots,
-// blockDim.y rows per block, rows strided over the grid (at most one wave of
-// CTAs, so a dependent launch is released as soon as every CTA has started).
+// Every query head of a token rotates its pairs by the same angles, so a work
+// item is (token t, slot c, group of kQkvHeads heads): one cos/sin for the
+// group, then the group's pairs loaded together and rotated. Items are
+// strided over the grid.
 template <int HD>
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(kQkvThreads)
 qkv_post_kernel(const float* __restrict__ q, int64_t q_tok_stride, const int32_t* __restrict__ pos,
-                int n_head, int M, __half* __restrict__ q16, float* __restrict__ q32,
+                int n_tok, int n_head, __half* __restrict__ q16, float* __restrict__ q32,
                 const __grid_constant__ RopeTable tb) {
     // Launched with programmatic stream serialization: wait until the grids
     // before this one on the stream are complete and their writes visible. A
@@ -81,53 +82,74 @@ qkv_post_kernel(const float* __restrict__ q, int64_t q_tok_stride, const int32_t
     // waits for this grid's completion before it reads the rows.
     asm volatile("griddepcontrol.wait;" ::: "memory");
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    const int c = threadIdx.x;                 // slot 0 .. HD/2-1
     // the table in shared memory: indexing the parameter copy with a
     // per-thread slot would serialise every access
     __shared__ RopeTable stb;
-    if (threadIdx.y == 0) {
-        stb.turns[c] = tb.turns[c];
-        if (c == 0) {
-            stb.mscale = tb.mscale;
-            stb.q_scale = tb.q_scale;
-            stb.half = tb.half;
-            stb.n_dims = tb.n_dims;
-        }
+    for (int c = threadIdx.x; c < HD / 2; c += blockDim.x) stb.turns[c] = tb.turns[c];
+    if (threadIdx.x == 0) {
+        stb.mscale = tb.mscale;
+        stb.q_scale = tb.q_scale;
+        stb.half = tb.half;
+        stb.n_dims = tb.n_dims;
     }
     __syncthreads();
-    for (int r = blockIdx.x * blockDim.y + threadIdx.y; r < M; r += gridDim.x * blockDim.y) {
-        const int t = r / n_head, h = r - t * n_head;
-        const float* qrow = q + (int64_t)t * q_tok_stride + (int64_t)h * HD;
+    constexpr int SLOTS = HD / 2;
+    const int groups = (n_head + kQkvHeads - 1) / kQkvHeads;
+    const int64_t items = (int64_t)n_tok * groups * SLOTS;
+    const float q_scale = stb.q_scale;
+    for (int64_t it = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; it < items;
+         it += (int64_t)gridDim.x * blockDim.x) {
+        const int c = (int)(it % SLOTS);                    // consecutive threads: consecutive slots
+        const int64_t tg = it / SLOTS;
+        const int t = (int)(tg / groups), h0 = (int)(tg - (int64_t)t * groups) * kQkvHeads;
         int d0, d1;
-        float y0, y1;
-        rope_slot(qrow, c, __ldg(pos + t), stb, d0, d1, y0, y1);
-        __half* orow = q16 + (int64_t)r * HD;
-        orow[d0] = __float2half_rn(y0);
-        orow[d1] = __float2half_rn(y1);
-        if (q32) {
-            float* frow = q32 + (int64_t)r * HD;
-            frow[d0] = y0;
-            frow[d1] = y1;
+        rope_slot_dims(c, stb, d0, d1);
+        const float* qh = q + (int64_t)t * q_tok_stride + (int64_t)h0 * HD;
+        float x0[kQkvHeads], x1[kQkvHeads];
+#pragma unroll
+        for (int u = 0; u < kQkvHeads; ++u) {
+            x0[u] = h0 + u < n_head ? __ldg(qh + u * HD + d0) : 0.f;
+            x1[u] = h0 + u < n_head ? __ldg(qh + u * HD + d1) : 0.f;
+        }
+        const bool rot = c < stb.half;
+        float cs = 0.f, sn = 0.f;
+        if (rot) rope_cs(__ldg(pos + t), stb.turns[c], stb.mscale, cs, sn);
+        const int64_t r0 = (int64_t)t * n_head + h0;       // t-major row of head h0
+#pragma unroll
+        for (int u = 0; u < kQkvHeads; ++u) {
+            if (h0 + u >= n_head) break;
+            // the same operations as rope_slot_apply, so the bits match
+            const float y0 = rot ? rope_lo(x0[u], x1[u], cs, sn, q_scale) : __fmul_rn(x0[u], q_scale);
+            const float y1 = rot ? rope_hi(x0[u], x1[u], cs, sn, q_scale) : __fmul_rn(x1[u], q_scale);
+            __half* orow = q16 + (r0 + u) * HD;
+            orow[d0] = __float2half_rn(y0);
+            orow[d1] = __float2half_rn(y1);
+            if (q32) {
+                float* frow = q32 + (r0 + u) * HD;
+                frow[d0] = y0;
+                frow[d1] = y1;
+            }
         }
     }
 }
 
-constexpr int kQkvMaxCtas = 1216;            // 8 CTAs of 256 threads on each of 152 SMs
+// at most 8 CTAs of 256 threads on each of 152 SMs: one wave, so a dependent
+// launch is released as soon as every CTA has started
+constexpr int kQkvMaxCtas = 1216;
 
 fr_status launch_qkv_post(const float* q, int64_t q_tok_stride, const int32_t* pos, int n_tok, int n_head,
                           int hd, const RopeTable& tb, uint16_t* q16_out, float* q32_out, cudaStream_t stream) {
-    const int M = n_tok * n_head;
-    const int slots = hd / 2;
-    const int rows_per_block = 256 / slots;
-    dim3 block(slots, rows_per_block);
-    dim3 grid(min((M + rows_per_block - 1) / rows_per_block, kQkvMaxCtas));
+    const int64_t items = (int64_t)n_tok * ((n_head + kQkvHeads - 1) / kQkvHeads) * (hd / 2);
+    const int threads = items < kQkvThreads ? (int)((items + 31) / 32 * 32) : kQkvThreads;
+    int64_t ctas = (items + threads - 1) / threads;
+    if (ctas > kQkvMaxCtas) ctas = kQkvMaxCtas;
     __half* o16 = reinterpret_cast<__half*>(q16_out);
     // programmatic dependent launch: this grid may be scheduled while the
     // previous one on the stream finishes (the kernel waits before any access)
     cudaLaunchConfig_t cfg;
     memset(&cfg, 0, sizeof(cfg));
-    cfg.gridDim = grid;
-    cfg.blockDim = block;
+    cfg.gridDim = dim3((unsigned)ctas);
+    cfg.blockDim = dim3(threads);
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -136,9 +158,9 @@ fr_status launch_qkv_post(const float* q, int64_t q_tok_stride, const int32_t* p
     cfg.numAttrs = 1;
     cudaError_t e;
     switch (hd) {
-        case 64: e = cudaLaunchKernelEx(&cfg, qkv_post_kernel<64>, q, q_tok_stride, pos, n_head, M, o16, q32_out, tb); break;
-        case 128: e = cudaLaunchKernelEx(&cfg, qkv_post_kernel<128>, q, q_tok_stride, pos, n_head, M, o16, q32_out, tb); break;
-        default: e = cudaLaunchKernelEx(&cfg, qkv_post_kernel<256>, q, q_tok_stride, pos, n_head, M, o16, q32_out, tb); break;
+        case 64: e = cudaLaunchKernelEx(&cfg, qkv_post_kernel<64>, q, q_tok_stride, pos, n_tok, n_head, o16, q32_out, tb); break;
+        case 128: e = cudaLaunchKernelEx(&cfg, qkv_post_kernel<128>, q, q_tok_stride, pos, n_tok, n_head, o16, q32_out, tb); break;
+        default: e = cudaLaunchKernelEx(&cfg, qkv_post_kernel<256>, q, q_tok_stride, pos, n_tok, n_head, o16, q32_out, tb); break;
     }
     return e == cudaSuccess ? FR_OK : FR_ERR_CUDA;
 }
