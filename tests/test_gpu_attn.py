@@ -82,7 +82,7 @@ def test_ragged_kv_and_strides(n_kv, hd):
 
 
 @pytest.mark.parametrize("hd", [64, 128, 256])
-@pytest.mark.parametrize("n_head,n_tok", [(1, 1), (32, 16), (3, 11)])
+@pytest.mark.parametrize("n_head,n_tok", [(1, 1), (32, 16), (3, 11), (512, 1)])
 def test_edge_shapes(hd, n_head, n_tok):
     w = Workload("edge", n_head=n_head, n_tok=n_tok, hd=hd, n_kv=777,
                  rope=RopeParams(n_dims=hd, freq_base=10000.0),

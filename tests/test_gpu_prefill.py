@@ -61,6 +61,38 @@ def test_prefill_fused_equals_two_call():
     assert torch.equal(a, b)
 
 
+def _sampled_rows(w, n_random, seed):
+    rng = np.random.default_rng(seed)
+    toks = np.unique(np.concatenate([[0, w.n_tok - 1], rng.integers(0, w.n_tok, size=6)]))
+    return np.unique(np.concatenate([toks * w.n_head, toks * w.n_head + w.n_head - 1,
+                                     rng.integers(0, w.M, size=n_random)]))
+
+
+def test_largest_window_sampled_rows():
+    """The largest window the API takes: 8192 tokens x 8 heads = 65536 query
+    rows (512 row tiles) against 8192 keys, causal; the oracle checks a sample
+    of rows (first and last head of sampled tokens, plus random rows)."""
+    w = Workload("prefill_max", n_head=8, n_tok=8192, hd=128, n_kv=8192, n_kv_real=8192,
+                 rope=RopeParams(n_dims=128, freq_base=10000.0), positions=tuple(range(8192)),
+                 mask_kind="causal", seed=13)
+    d = to_device(w)
+    o = _rows(run_fused(w, d))
+    rows = _sampled_rows(w, 24, 13)
+    assert_close(o[rows], oracle_out(w, rows=rows), "65536-row window")
+
+
+def test_many_heads_one_kv_head_sampled_rows():
+    """4096 query heads sharing the KV head, 16 tokens: 65536 rows, ragged
+    KV length and a random mask."""
+    w = Workload("heads_max", n_head=4096, n_tok=16, hd=64, n_kv=300, n_kv_real=300,
+                 rope=RopeParams(n_dims=64, freq_base=10000.0), positions=tuple(range(284, 300)),
+                 mask_kind="random5", seed=14)
+    d = to_device(w)
+    o = _rows(run_fused(w, d))
+    rows = _sampled_rows(w, 24, 14)
+    assert_close(o[rows], oracle_out(w, rows=rows), "4096 heads x 16 tokens")
+
+
 def test_window_too_wide_is_rejected():
     # 4 heads: a 128-row tile spans 32 tokens, more than the 16-token mask window
     w = Workload("prefill_narrow", n_head=4, n_tok=40, hd=64, n_kv=64, n_kv_real=64,
