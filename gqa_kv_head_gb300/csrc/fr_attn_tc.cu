@@ -718,7 +718,7 @@ attn_tc_kernel(const __grid_constant__ TcArgs a, const __grid_constant__ Maps mp
 
 // Merge of the split states written in merge-kernel mode. A unit is one (row,
 // 128-column chunk); it gets nw warps (one per split when that fits the GPU in
-// one wave, else one per 8 splits, see launch_merge) and a CTA of up to
+// one wave, else one per 6 splits, see launch_merge) and a CTA of up to
 // kMergeWarps warps holds several units. Warp w of a unit takes splits
 // w, w + nw, ... (at most a handful each, so the loads of the whole CTA are in
 // flight together). Each warp weighs its splits by 2^(m_s - m_w) against its
@@ -726,7 +726,7 @@ attn_tc_kernel(const __grid_constant__ TcArgs a, const __grid_constant__ Maps mp
 // against the row maximum. The order of every sum is fixed: the result does
 // not depend on timing.
 constexpr int kMergeWarps = 32;
-constexpr int kMergeSplitsPerWarp = 8;          // nw = ceil(splits / 8) warps per unit
+constexpr int kMergeSplitsPerWarp = 6;          // nw = ceil(splits / 6) warps per unit
 
 template <int HD>
 __global__ void __launch_bounds__(kMergeWarps * 32)
@@ -899,7 +899,7 @@ fr_status launch_merge(const float* part_o, const float2* part_ml, float* out, i
         return FR_ERR_CUDA;
     // Warps per unit and units per CTA. When one warp per split fits the GPU in
     // one wave, take that (the fewest dependent loads per warp). Otherwise up to
-    // 8 splits per warp (fewer instructions per split), with few enough units
+    // 6 splits per warp (fewer instructions per split), with few enough units
     // per CTA that the grid still covers the SMs.
     int nw, upc;
     if ((int64_t)units * splits <= (int64_t)sms * kMergeWarps && splits <= kMergeWarps) {
