@@ -23,7 +23,7 @@ struct TcArgs {
     unsigned* status;
     int has_mask;
     int n_tok, n_head, M, n_kv;
-    int n_tiles;              // KV tiles of tile_keys(hd) keys
+    int n_tiles;              // KV tiles of tile_keys(...) keys
     int tiles_per_split;
     int n_clusters;           // clusters per row tile
     int C;                    // CTAs per cluster (splits per cluster)
@@ -43,9 +43,10 @@ struct TcLaunch {
     const void* mask;
     int64_t k_rs, v_rs, m_rs;
     int row_tiles, splits;
+    int bn;                   // keys per KV tile (tile_keys)
 };
 
-int tile_keys(int hd);
+int tile_keys(int hd, int n_kv, int row_tiles, int num_sms);
 fr_status launch_tc(const TcLaunch& L, int hd, cudaStream_t stream);
 // Merge of the split states written in merge-kernel mode (programmatic
 // dependent launch after the attention grid).

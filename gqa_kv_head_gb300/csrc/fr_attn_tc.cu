@@ -70,13 +70,21 @@ constexpr uint32_t kTmemCols = 512;
 constexpr int kOutBoxRows = 32;              // rows per TMA store box of the split states
 static_assert(kOutBoxRows == 32, "one box block = the 32 rows of one softmax warp");
 
-template <int HD>
+// Keys per KV tile: 64, or 128 at hd 128 for long KV ranges (half the S MMA
+// instructions per key: the N = 64 QK^T MMAs run at ~40 % of the tensor
+// peak). At hd 256 a 128-key K tile does not fit next to Q and a two-deep ring.
+template <int HD, int BN_>
 struct Cfg {
-    static constexpr int BN = 64;                          // keys per tile
+    static constexpr int BN = BN_;
+    static_assert(BN == 64 || (BN == 128 && HD == 128), "tile shapes");
+    // At BN = 128 the f16 P_hi / P_lo words go over the S columns the softmax
+    // thread has just read (TMEM: O, then two S buffers); else P has its own
+    // columns.
+    static constexpr bool PALIAS = BN == 128;
     // Separate rings for K, V and mask tiles: a K slot frees when S_j is
     // computed, a V slot when PV_j is, a mask slot when the softmax has read
     // it, so K tiles run ahead of the V tiles they travel with.
-    static constexpr int KS = HD == 256 ? 2 : (HD == 128 ? 3 : 8);   // K slots
+    static constexpr int KS = HD == 64 ? 8 : (HD == 128 && BN == 64 ? 3 : 2);   // K slots
     static constexpr int VS = KS;                                     // V slots
     static constexpr int MS = 4;                                      // mask slots
     static constexpr int NB = HD / 64;                     // 128-byte column boxes per row
@@ -121,9 +129,15 @@ struct Cfg {
     // TMEM columns
     static constexpr int TM_O = 0;
     static constexpr int TM_S = HD;
-    static constexpr int TM_P = HD + 2 * BN;               // P_hi, 2 x BN/2 columns
-    static constexpr int TM_PL = TM_P + BN;                // P_lo, 2 x BN/2 columns
-    static_assert(TM_PL + BN <= (int)kTmemCols, "TMEM budget");
+    static constexpr int TM_P = HD + 2 * BN;               // P_hi, 2 x BN/2 columns (not PALIAS)
+    static constexpr int TM_PL = TM_P + BN;                // P_lo, 2 x BN/2 columns (not PALIAS)
+    static_assert((PALIAS ? TM_S + 2 * BN : TM_PL + BN) <= (int)kTmemCols, "TMEM budget");
+    // TMEM column of softmax half h's f16 P_hi (lo = 0) or P_lo (lo = 1) words
+    // for S buffer b: BN/4 columns (two keys per 32-bit column)
+    __host__ __device__ static constexpr int p_col(int b, int h, int lo) {
+        return PALIAS ? TM_S + b * BN + h * (BN / 2) + lo * (BN / 4)
+                      : (lo ? TM_PL : TM_P) + b * (BN / 2) + h * (BN / 4);
+    }
     static_assert(K_BYTES % 1024 == 0 && MASK_BYTES % 1024 == 0 && Q_BYTES % 1024 == 0,
                   "1024-B alignment of swizzled tiles");
     static_assert(SMEM <= 232448, "shared memory budget");
@@ -148,10 +162,10 @@ __device__ __forceinline__ void softmax_bar_sync() {
     asm volatile("bar.sync 5, %0;" :: "n"(kSmaxThreads) : "memory");
 }
 
-template <int HD>
+template <int HD, int BN_>
 __global__ void __launch_bounds__(kThreads, 1)
 attn_tc_kernel(const __grid_constant__ TcArgs a, const __grid_constant__ Maps mp) {
-    using C = Cfg<HD>;
+    using C = Cfg<HD, BN_>;
     constexpr int BN = C::BN;
     constexpr int HB = BN / 2;                           // S columns per softmax half
     constexpr int OH = HD / 2;                           // O columns per softmax half
@@ -379,13 +393,15 @@ attn_tc_kernel(const __grid_constant__ TcArgs a, const __grid_constant__ Maps mp
                 wait(bar(C::B_VFULL + i % C::VS), (i / C::VS) & 1);
                 tc_fence_after();
                 const uint32_t v_base = smem_addr(sV(i % C::VS));
-                const uint32_t p_tm = tbase + C::TM_P + (i & 1) * HB;
-                const uint32_t pl_tm = tbase + C::TM_PL + (i & 1) * HB;
 #pragma unroll
                 for (int ks = 0; ks < BN / 16; ++ks) {
+                    // keys [16 ks, 16 ks + 16): softmax half h, k-step kk within it
+                    const int h = ks / (BN / 32), kk = ks % (BN / 32);
+                    const uint32_t p_tm = tbase + C::p_col(i & 1, h, 0) + kk * 8;
+                    const uint32_t pl_tm = tbase + C::p_col(i & 1, h, 1) + kk * 8;
                     const uint64_t vd = sdesc_sw128(v_base + ks * 2048, C::KV_BOX, 1024);
-                    mma_ts(tbase + C::TM_O, p_tm + ks * 8, vd, idO, (i > 0 || ks > 0) ? 1u : 0u);
-                    mma_ts(tbase + C::TM_O, pl_tm + ks * 8, vd, idO, 1u);
+                    mma_ts(tbase + C::TM_O, p_tm, vd, idO, (i > 0 || ks > 0) ? 1u : 0u);
+                    mma_ts(tbase + C::TM_O, pl_tm, vd, idO, 1u);
                 }
                 mma_commit(bar(C::B_ODONE));
                 mma_commit(bar(C::B_VEMPTY + i % C::VS));
@@ -408,7 +424,10 @@ attn_tc_kernel(const __grid_constant__ TcArgs a, const __grid_constant__ Maps mp
             float pm = -INFINITY;
             const int j0 = (t0 + i) * BN + c_base;
             if (quad_active) {
-                tmem_ld_x32(tbase + lane_base + C::TM_S + (i & 1) * BN + c_base, reinterpret_cast<uint32_t*>(x));
+#pragma unroll
+                for (int c = 0; c < HB; c += 32)
+                    tmem_ld_x32(tbase + lane_base + C::TM_S + (i & 1) * BN + c_base + c,
+                                reinterpret_cast<uint32_t*>(x) + c);
                 tmem_wait_ld();
                 const float kq = a.kq_log2;
                 if (a.has_mask) {
@@ -471,20 +490,23 @@ attn_tc_kernel(const __grid_constant__ TcArgs a, const __grid_constant__ Maps mp
                 }
                 const float m_sub = m_new == -INFINITY ? 0.f : m_new;
                 float sum4[4] = {0.f, 0.f, 0.f, 0.f};
-                uint32_t pk[HB / 2], pl[HB / 2];
 #pragma unroll
-                for (int c = 0; c < HB; c += 2) {
-                    const float p0 = ex2(x[c] - m_sub), p1 = ex2(x[c + 1] - m_sub);
-                    sum4[(c >> 1) & 3] += p0 + p1;
-                    const uint32_t hbits = pack_half2(p0, p1);
-                    const float2 hf = __half22float2(*reinterpret_cast<const __half2*>(&hbits));
-                    pk[c / 2] = hbits;
-                    pl[c / 2] = pack_half2(p0 - hf.x, p1 - hf.y);
+                for (int cc = 0; cc < HB; cc += 32) {       // 32 columns at a time
+                    uint32_t pk[16], pl[16];
+#pragma unroll
+                    for (int c = 0; c < 32; c += 2) {
+                        const float p0 = ex2(x[cc + c] - m_sub), p1 = ex2(x[cc + c + 1] - m_sub);
+                        sum4[(c >> 1) & 3] += p0 + p1;
+                        const uint32_t hbits = pack_half2(p0, p1);
+                        const float2 hf = __half22float2(*reinterpret_cast<const __half2*>(&hbits));
+                        pk[c / 2] = hbits;
+                        pl[c / 2] = pack_half2(p0 - hf.x, p1 - hf.y);
+                    }
+                    tmem_st_x16(tbase + lane_base + C::p_col(i & 1, half, 0) + cc / 2, pk);
+                    tmem_st_x16(tbase + lane_base + C::p_col(i & 1, half, 1) + cc / 2, pl);
                 }
                 const float sum = (sum4[0] + sum4[1]) + (sum4[2] + sum4[3]);
                 l_part = fmaf(l_part, alpha, sum);
-                tmem_st_x16(tbase + lane_base + C::TM_P + (i & 1) * HB + half * (HB / 2), pk);
-                tmem_st_x16(tbase + lane_base + C::TM_PL + (i & 1) * HB + half * (HB / 2), pl);
                 tmem_wait_st();
             }
             m_ref = m_new;
@@ -970,26 +992,35 @@ static bool encode_2d_f32(CUtensorMap* m, void* base, uint64_t inner, uint64_t r
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int HD>
+template <int HD, int BN>
 static cudaError_t ensure_attr(int dev) {
     static unsigned long long done = 0ull;
     if (dev < 64 && (__atomic_load_n(&done, __ATOMIC_ACQUIRE) >> dev & 1ull)) return cudaSuccess;
-    cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<HD>::SMEM);
+    cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<HD, BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         Cfg<HD, BN>::SMEM);
     if (e == cudaSuccess && dev < 64) __atomic_fetch_or(&done, 1ull << dev, __ATOMIC_RELEASE);
     return e;
 }
 
-int tile_keys(int hd) { return hd == 256 ? Cfg<256>::BN : (hd == 128 ? Cfg<128>::BN : Cfg<64>::BN); }
+// 128-key tiles at hd 128 when there is at least one for each SM of a row
+// tile's share (measured: 65536 keys 1.0-1.5 us faster per call, 32768 keys on
+// 4 row tiles 3.3 us faster; even at 16384 keys; 1.7-2.4 us slower at 4096
+// keys, where they would halve the CTAs).
+int tile_keys(int hd, int n_kv, int row_tiles, int num_sms) {
+    if (hd != 128) return 64;
+    const int share = row_tiles > 0 ? num_sms / row_tiles : num_sms;
+    return n_kv / 128 >= share ? 128 : 64;
+}
 
-template <int HD>
+template <int HD, int BN_>
 static fr_status launch(const TcLaunch& L, cudaStream_t stream) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return FR_ERR_CUDA;
-    if (ensure_attr<HD>(dev) != cudaSuccess) return FR_ERR_CUDA;
+    if (ensure_attr<HD, BN_>(dev) != cudaSuccess) return FR_ERR_CUDA;
     Maps mp;
     memset(&mp, 0, sizeof(mp));
     const TcArgs& a = L.args;
-    constexpr int BN = Cfg<HD>::BN;
+    constexpr int BN = Cfg<HD, BN_>::BN;
     if (!encode_2d(&mp.k, L.k, HD, a.n_kv, L.k_rs, 64, BN)) return FR_ERR_CUDA;
     if (!encode_2d(&mp.v, L.v, HD, a.n_kv, L.v_rs, 64, BN)) return FR_ERR_CUDA;
     if (a.has_mask &&
@@ -1004,7 +1035,7 @@ static fr_status launch(const TcLaunch& L, cudaStream_t stream) {
     memset(&cfg, 0, sizeof(cfg));
     cfg.gridDim = dim3(L.row_tiles, L.splits, 1);
     cfg.blockDim = dim3(kThreads, 1, 1);
-    cfg.dynamicSmemBytes = Cfg<HD>::SMEM;
+    cfg.dynamicSmemBytes = Cfg<HD, BN_>::SMEM;
     cfg.stream = stream;
     cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -1015,15 +1046,15 @@ static fr_status launch(const TcLaunch& L, cudaStream_t stream) {
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = L.pdl ? 2 : 1;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, attn_tc_kernel<HD>, a, mp);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, attn_tc_kernel<HD, BN_>, a, mp);
     return e == cudaSuccess ? FR_OK : FR_ERR_CUDA;
 }
 
 fr_status launch_tc(const TcLaunch& L, int hd, cudaStream_t stream) {
     switch (hd) {
-        case 64: return launch<64>(L, stream);
-        case 128: return launch<128>(L, stream);
-        default: return launch<256>(L, stream);
+        case 64: return launch<64, 64>(L, stream);
+        case 128: return L.bn == 128 ? launch<128, 128>(L, stream) : launch<128, 64>(L, stream);
+        default: return launch<256, 64>(L, stream);
     }
 }
 

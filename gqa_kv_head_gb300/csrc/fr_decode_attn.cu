@@ -421,13 +421,15 @@ static size_t workspace_bytes_for(int n_tok, int n_head, int hd, int n_kv) {
 // CTAs as are co-resident for that cluster size (1 CTA per SM).
 struct TcPlan {
     int row_tiles, n_tiles, C, n_clusters, splits, tiles_per_split;
+    int bn;                // keys per KV tile
     int merge_kernel;      // 1: separate merge kernel (C == 1, splits over the whole GPU)
 };
 
 static TcPlan make_tc_plan(int M, int hd, int n_kv, int num_sms, int force_splits, int force_cluster) {
     TcPlan p;
-    const int bn = tc::tile_keys(hd);
     p.row_tiles = (M + 127) / 128;
+    const int bn = tc::tile_keys(hd, n_kv, p.row_tiles, num_sms);
+    p.bn = bn;
     p.n_tiles = (n_kv + bn - 1) / bn;
     // clusters of 8 for one row tile; with several row tiles (whose CTAs share
     // each K/V tile through L2) clusters of 4, which fit more CTAs per GPU
@@ -611,6 +613,7 @@ static fr_status decode_attn_impl(const uint16_t* q16, const float* q, int64_t q
         L.m_rs = m_rs;
         L.row_tiles = p.row_tiles;
         L.splits = p.splits;
+        L.bn = p.bn;
         const fr_status st = tc::launch_tc(L, hd, stream);
         if (st != FR_OK || !p.merge_kernel) return st;
         return tc::launch_merge(a.part_o, a.part_ml, out, M, p.splits, hd, stream);

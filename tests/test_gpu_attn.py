@@ -81,6 +81,22 @@ def test_ragged_kv_and_strides(n_kv, hd):
     assert_close(out, oracle_out(w), w.name)
 
 
+def test_128_key_tiles_ragged_tail():
+    """hd 128 over a long KV range takes 128-key tiles (P written over S in
+    TMEM); 20037 keys leave a last tile of 69 keys, across the boundary of the
+    two softmax halves. Padded strides, random mask, extra Q heads."""
+    w = Workload("tile128", n_head=8, n_tok=16, hd=128, n_kv=20037,
+                 rope=RopeParams(n_dims=128, freq_base=10000.0),
+                 positions=tuple(range(20021, 20037)), mask_kind="random5", seed=15)
+    d = to_device(w, k_pad=16, mask_pad=8, q_extra_heads=2)
+    out = _out_rows(run_fused(w, d))
+    assert_close(out, oracle_out(w), "128-key tiles, ragged tail")
+    ref = oracle_out(w)
+    for splits, cluster in ((1, 1), (5, 1), (8, 8)):
+        o = _out_rows(run_fused(w, d, splits=splits, cluster=cluster))
+        assert_close(o, ref, f"128-key tiles, splits={splits} cluster={cluster}")
+
+
 @pytest.mark.parametrize("hd", [64, 128, 256])
 @pytest.mark.parametrize("n_head,n_tok", [(1, 1), (32, 16), (3, 11), (512, 1)])
 def test_edge_shapes(hd, n_head, n_tok):
