@@ -85,10 +85,12 @@ def test_kv_append_identity_at_pos0_bitwise():
     assert np.array_equal(kc[5:5 + w.n_tok].view(np.uint16), want.view(np.uint16))
 
 
-def test_append_then_fused_attention_matches_oracle():
+@pytest.mark.parametrize("name", ["pi05", "long_decode"])
+def test_append_then_fused_attention_matches_oracle(name):
     """The new K/V rows written by fr_kv_append are what the following fused
-    fr_decode_attn on the same stream attends to."""
-    w = named_config("pi05")
+    fr_decode_attn on the same stream attends to (long decode: hd 128 over
+    32768 keys, the 128-key tile path)."""
+    w = named_config(name)
     rng = np.random.default_rng(8)
     hd = w.hd
     kc0, vc0 = host_kv(w)
@@ -96,7 +98,7 @@ def test_append_then_fused_attention_matches_oracle():
     v_new = rng.standard_normal((w.n_tok, hd)).astype(np.float32) * 0.5
     pos = w.pos()
     row0 = int(pos[0])
-    pad = (w.n_kv_real, w.n_kv)
+    pad = (w.n_kv_real, w.n_kv) if w.n_kv_real < w.n_kv else None
     okc, ovc, _, _ = oracle.kv_append(kc0, vc0, k_new, v_new, pos, w.rope, row0, pad)
     want = oracle.decode_attn(w.q(), pos, okc, ovc, w.mask(), w.rope, w.q_scale, w.kq_scale)
     kc = torch.from_numpy(kc0.copy()).cuda()
@@ -110,4 +112,4 @@ def test_append_then_fused_attention_matches_oracle():
                              pos=d_pos, rope=w.rope, q_scale=w.q_scale,
                              mask=torch.from_numpy(w.mask()).cuda(), kq_scale=w.kq_scale, stream=st)
     st.synchronize()
-    assert_close(out.cpu().numpy().reshape(w.n_tok * w.n_head, hd), want, "append + attention")
+    assert_close(out.cpu().numpy().reshape(w.n_tok * w.n_head, hd), want, f"{name}: append + attention")
