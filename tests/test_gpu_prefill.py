@@ -93,6 +93,18 @@ def test_many_heads_one_kv_head_sampled_rows():
     assert_close(o[rows], oracle_out(w, rows=rows), "4096 heads x 16 tokens")
 
 
+def test_more_row_tiles_than_sms_short_kv():
+    """256 row tiles (more than SMs) over only 50 keys at hd 128: 128-key tiles
+    whose second softmax half lies wholly past the last key."""
+    w = Workload("tiles_short_kv", n_head=2048, n_tok=16, hd=128, n_kv=50, n_kv_real=50,
+                 rope=RopeParams(n_dims=128, freq_base=10000.0), positions=tuple(range(34, 50)),
+                 mask_kind="random5", seed=16)
+    d = to_device(w)
+    o = _rows(run_fused(w, d))
+    rows = _sampled_rows(w, 24, 16)
+    assert_close(o[rows], oracle_out(w, rows=rows), "256 row tiles, 50 keys")
+
+
 def test_window_too_wide_is_rejected():
     # 4 heads: a 128-row tile spans 32 tokens, more than the 16-token mask window
     w = Workload("prefill_narrow", n_head=4, n_tok=40, hd=64, n_kv=64, n_kv_real=64,
