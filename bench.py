@@ -3,7 +3,7 @@
 one fr_decode_attn call per step) on synthetic inputs of the documented
 workloads.
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--config pi05]
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config sweep:256:16:65536]
                     [--impl ours|reference] [--no-cpu-baseline]
 
 Prints ONE JSON line (rank 0). `value` is device time per call in µs (lower is
@@ -22,6 +22,7 @@ import json
 import math
 import os
 import re
+import statistics
 import subprocess
 import sys
 import time
@@ -30,6 +31,8 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 L2_BYTES = 129 * 1024 * 1024
+REPEATS = 5                     # timed repeats; the line reports their median
+DEFAULT_CONFIG = "sweep:256:16:65536"   # the largest single-GPU workload (64 MiB of K/V)
 METRIC = "decode-attn µs/call (fused qkv_post + attention) and effective K/V HBM GB/s"
 
 
@@ -78,13 +81,14 @@ def attention_flops(w):
     return 4 * w.M * w.hd * w.n_kv
 
 
-def roofline_entry(w, attn_us, attn_bytes, peaks, traffic, kernels):
+def roofline_entry(w, attn_us, attn_bytes, peaks, traffic, traffic_source, kernels):
     """Roofline of the attention launch(es): HBM-bound unless its flops per
     algorithmic byte exceed the ridge point of the measured peaks."""
     flops = attention_flops(w)
     gbs = attn_bytes / (attn_us * 1e-6) / 1e9
     ridge = peaks["tflops"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
-    base = {"traffic": traffic, "kernel": f"{kernels} (decode attention on f16 Q rows, one call)",
+    base = {"traffic": traffic, "traffic_source": traffic_source,
+            "kernel": f"{kernels} (decode attention on f16 Q rows, one call)",
             "kernel_us_per_launch": attn_us, "algorithmic_bytes_per_launch": attn_bytes,
             "algorithmic_flops_per_launch": flops}
     if flops / attn_bytes > ridge:
@@ -108,16 +112,21 @@ def kernel_source_hash():
 
 
 def ncu_traffic(config):
-    """DRAM bytes per launch from the committed ncu summary for this workload,
-    valid only while the kernel sources are unchanged since the capture."""
-    p = os.path.join(ROOT, "profiles", f"fr_decode_attn_{config}.md")
+    """DRAM bytes per call (dram__bytes_read.sum + dram__bytes_write.sum of the
+    attention and merge launches) from the committed ncu summary for this
+    workload, with where they come from; (None, reason) once the kernel sources
+    differ from those the counters were taken on."""
+    name = f"fr_decode_attn_{config}.md"
+    p = os.path.join(ROOT, "profiles", name)
     if not os.path.exists(p):
-        return None
+        return None, f"no ncu summary profiles/{name}"
     txt = open(p).read()
     m = re.search(r"traffic_bytes_per_launch:\s*(\d+)\s+source_sha:\s*([0-9a-f]+)", txt)
-    if not m or m.group(2) != kernel_source_hash():
-        return None
-    return int(m.group(1))
+    if not m:
+        return None, f"profiles/{name} holds no traffic line"
+    if m.group(2) != kernel_source_hash():
+        return None, f"profiles/{name} was taken at kernel source hash {m.group(2)}, not the current one"
+    return int(m.group(1)), f"ncu capture in profiles/{name} at kernel source hash {m.group(2)} (not measured in this run)"
 
 
 class ClockSampler:
@@ -188,6 +197,61 @@ def cpu_oracle_time(config, budget_s, threads=1):
         raise RuntimeError("cpu oracle run failed: " + r.stderr[-2000:])
     d = json.loads(r.stdout.strip().splitlines()[-1])
     return d["us"], d["calls"]
+
+
+class CycleTimer:
+    """Times exactly `steps` calls with CUDA events on `stream`. Call i of the
+    cycle reads replica i % n_rep; the cycle graph holds G calls (G a multiple
+    of n_rep, at least 64), so `steps` = q * G + r calls are q replays of it and
+    one replay of a graph of its first r calls. After each timed region the
+    remaining G - r calls of the cycle run untimed (and before the first one, a
+    whole cycle), so the cyclic order, and with it the L2 distance between two
+    reads of one replica, never breaks."""
+
+    def __init__(self, call, reps, n_rep, steps, stream):
+        import torch
+        self.stream = stream
+        self.G = n_rep * max(1, math.ceil(64 / n_rep))
+        self.q, self.r = divmod(steps, self.G)
+
+        def capture(lo, hi):
+            if hi <= lo:
+                return None
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                for i in range(lo, hi):
+                    call(reps[i % n_rep], stream)
+            return g
+        self.g_cycle = capture(0, self.G) if self.q else None
+        self.g_head = capture(0, self.r)
+        self.g_tail = capture(self.r, self.G)
+        if self.g_cycle is None:
+            self.g_cycle_w = capture(0, self.G)
+        else:
+            self.g_cycle_w = self.g_cycle
+
+    def warm(self):
+        import torch
+        with torch.cuda.stream(self.stream):
+            self.g_cycle_w.replay()
+        self.stream.synchronize()
+
+    def time_ms(self):
+        import torch
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        self.stream.synchronize()
+        with torch.cuda.stream(self.stream):
+            e0.record(self.stream)
+            for _ in range(self.q):
+                self.g_cycle.replay()
+            if self.g_head is not None:
+                self.g_head.replay()
+            e1.record(self.stream)
+            if self.g_tail is not None:
+                self.g_tail.replay()
+        self.stream.synchronize()
+        return e0.elapsed_time(e1)
 
 
 def max_over_ranks(x, dist, device):
@@ -278,24 +342,17 @@ def run_ours(args, rank, world, local_rank):
             call(reps[i % n_rep], stream)
     stream.synchronize()
 
-    # --- graph of G calls rotating over the replicas --------------------------
-    G = min(args.steps, max(n_rep, 1000))
-    def capture(n):
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g, stream=stream):
-            for i in range(n):
-                call(reps[i % n_rep], stream)
-        return g
-    g_full = capture(G)
-    rem = args.steps % G
-    g_rem = capture(rem) if rem else None
-    n_full = args.steps // G
-    with torch.cuda.stream(stream):
-        g_full.replay()                       # graph warm-up
-    stream.synchronize()
+    # --- graphs that rotate over the replicas in one fixed cycle -------------
+    # Call i of a cycle reads replica i % n_rep; a cycle is G calls (a multiple
+    # of n_rep). K timed calls = q full cycles + the first r calls of one, and
+    # between repeats the rest of that cycle runs untimed, so every timed call
+    # reads a replica last touched n_rep - 1 calls (> 2x L2 of other bytes)
+    # earlier, whatever K is.
+    timer = CycleTimer(call, reps, n_rep, args.steps, stream)
+    timer.warm()
 
-    # the dominant kernel alone: the attention on precomputed f16 Q rows, same
-    # replicas and launch shape, for the roofline's per-launch duration
+    # the dominant kernels alone: the attention (+ merge) on precomputed f16 Q
+    # rows, same replicas and launch shape, for the roofline's per-launch time
     for r in reps:
         r["q16"], _ = fr.qkv_post(r["q"], r["pos"], w.n_head, w.hd, w.rope, w.q_scale)
     torch.cuda.synchronize()
@@ -304,23 +361,9 @@ def run_ours(args, rank, world, local_rank):
         fr.decode_attn(r["k"], r["v"], w.n_tok, w.n_head, q16=r["q16"], mask=r["mask"],
                        kq_scale=w.kq_scale, out=out, workspace=ws, stream=st)
 
-    g_attn = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g_attn, stream=stream):
-        for i in range(G):
-            call_attn(reps[i % n_rep], stream)
-    with torch.cuda.stream(stream):
-        g_attn.replay()
-    stream.synchronize()
-    ka0 = torch.cuda.Event(enable_timing=True)
-    ka1 = torch.cuda.Event(enable_timing=True)
-    n_attn = max(1, min(n_full, 10))
-    with torch.cuda.stream(stream):
-        ka0.record(stream)
-        for _ in range(n_attn):
-            g_attn.replay()
-        ka1.record(stream)
-    stream.synchronize()
-    attn_us = ka0.elapsed_time(ka1) * 1000.0 / (n_attn * G)
+    attn_timer = CycleTimer(call_attn, reps, n_rep, args.steps, stream)
+    attn_timer.warm()
+    attn_us = statistics.median(attn_timer.time_ms() for _ in range(REPEATS)) * 1000.0 / args.steps
 
     # the K/V leg of qkv_post (the next layer of the path, timed beside it, not
     # part of `value`): n_tok new rows appended at the tail of each replica's
@@ -337,9 +380,10 @@ def run_ours(args, rank, world, local_rank):
         for i in range(3):
             call_kv(i, stream)
     stream.synchronize()
+    G_KV = 64
     g_kv = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g_kv, stream=stream):
-        for i in range(G):
+        for i in range(G_KV):
             call_kv(i, stream)
     with torch.cuda.stream(stream):
         g_kv.replay()
@@ -348,39 +392,33 @@ def run_ours(args, rank, world, local_rank):
         g_kv.replay()
         kv1.record(stream)
     stream.synchronize()
-    kv_append_us = kv0.elapsed_time(kv1) * 1000.0 / G
+    kv_append_us = kv0.elapsed_time(kv1) * 1000.0 / G_KV
     del kv_caches
 
     dist = None
     if world > 1:
         import torch.distributed as dist
     clocks = ClockSampler(local_rank)
-    ev0 = torch.cuda.Event(enable_timing=True)
-    ev1 = torch.cuda.Event(enable_timing=True)
     if dist:
         dist.barrier()
     torch.cuda.synchronize()
     clocks.start()
     time.sleep(0.15)
-    with torch.cuda.stream(stream):
-        ev0.record(stream)
-        for _ in range(n_full):
-            g_full.replay()
-        if g_rem is not None:
-            g_rem.replay()
-        ev1.record(stream)
-    stream.synchronize()
-    # keep the same replays running briefly so the sampler sees the load
+    rep_ms = []
+    for _ in range(REPEATS):
+        if dist:
+            dist.barrier()
+        torch.cuda.synchronize()
+        rep_ms.append(timer.time_ms())
+    # keep the same calls running briefly so the sampler sees the load
     t_end = time.perf_counter() + 0.6
-    with torch.cuda.stream(stream):
-        while time.perf_counter() < t_end:
-            g_full.replay()
-            stream.synchronize()
+    while time.perf_counter() < t_end:
+        timer.time_ms()
     clk = clocks.stop()
     torch.cuda.synchronize()
     if dist:
         dist.barrier()
-    ms = max_over_ranks(ev0.elapsed_time(ev1), dist, dev)
+    ms = max_over_ranks(statistics.median(rep_ms), dist, dev)
     us_per_call = ms * 1000.0 / args.steps
 
     # --- end to end through the public API with pinned host buffers ----------
@@ -449,15 +487,19 @@ def run_ours(args, rank, world, local_rank):
         "warmup": args.warmup, "ms_per_step": us_per_call / 1000.0, "higher_is_better": False,
         "scaling": "weak", "vs_baseline": None, "dtype": "f16", "data": "synthetic",
         "config": config_dict(w),
-        "timing": {"launch": f"CUDA graph of {G} back-to-back calls, replayed; each call = "
+        "timing": {"launch": f"CUDA graphs of back-to-back calls (cycle of {timer.G}, replayed); each call = "
                              f"qkv_post kernel + {attn_kernels} (programmatic dependent launches)",
                    "plan": plan,
-                   "l2": f"inputs rotated over {n_rep} replicas ({n_rep * per_rep / 2**20:.0f} MiB > 2x L2)",
+                   "repeats": REPEATS, "stat": f"median of {REPEATS} timed repeats of {args.steps} calls",
+                   "repeat_us_per_call": [x * 1000.0 / args.steps for x in rep_ms],
+                   "l2": f"every timed call reads its own replica, {n_rep} replicas ({n_rep * per_rep / 2**20:.0f} MiB) "
+                         f"in a fixed cycle: each call's inputs were last touched {n_rep - 1} calls "
+                         f"({(n_rep - 1) * per_rep / 2**20:.0f} MiB > 2x L2) earlier, at any step count",
                    "parallelism": "replicas only" if world > 1 else "1 GPU"},
         "calls_per_s_all_ranks": job_calls_per_s(world, args.steps, ms),
         "kv_gbs": kv_real_bytes / (us_per_call * 1e-6) / 1e9,
         "kv_frac_of_hbm": kv_real_bytes / (us_per_call * 1e-6) / 1e9 / peak,
-        "roofline": roofline_entry(w, attn_us, attn_bytes, peaks, ncu_traffic(w.name), attn_kernels),
+        "roofline": roofline_entry(w, attn_us, attn_bytes, peaks, *ncu_traffic(w.name), attn_kernels),
         "e2e": {"value": e2e_us, "unit": "us/call", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
         "gpu_launches": plan["launches"] * args.steps,
@@ -475,7 +517,7 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20000)
     ap.add_argument("--warmup", type=int, default=20)
-    ap.add_argument("--config", default="pi05",
+    ap.add_argument("--config", default=DEFAULT_CONFIG,
                     help="tiny | pi05 | c3 | long_decode | sweep:hd:n_tok:n_kv")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -46,9 +46,26 @@ def uniform(seed, stream, n, offset=0):
     return (x >> np.uint64(11)).astype(np.float64) * (2.0 ** -53)
 
 
-def normal(seed, stream, n, sigma=1.0):
-    """n standard normals (times sigma) in double, Box-Muller over index pairs."""
-    idx = np.arange(n, dtype=np.uint64)
+_CHUNK = 1 << 20
+
+
+def normal(seed, stream, n, sigma=1.0, offset=0):
+    """n standard normals (times sigma) in double, Box-Muller over index pairs
+    offset .. offset+n-1. Large requests are computed in chunks on a thread
+    pool (numpy releases the GIL); every value depends on its index only, so
+    the result is the same as in one piece."""
+    if n > 2 * _CHUNK:
+        from concurrent.futures import ThreadPoolExecutor
+        import os
+        out = np.empty(n, dtype=np.float64)
+
+        def fill(lo):
+            hi = min(n, lo + _CHUNK)
+            out[lo:hi] = normal(seed, stream, hi - lo, sigma, offset + lo)
+        with ThreadPoolExecutor(max_workers=min(16, os.cpu_count() or 1)) as ex:
+            list(ex.map(fill, range(0, n, _CHUNK)))
+        return out
+    idx = np.arange(offset, offset + n, dtype=np.uint64)
     with np.errstate(over="ignore"):
         u1 = (splitmix64_stream(seed, stream, idx * np.uint64(2)) >> np.uint64(11)).astype(np.float64) * (2.0 ** -53)
         u2 = (splitmix64_stream(seed, stream, idx * np.uint64(2) + np.uint64(1)) >> np.uint64(11)).astype(np.float64) * (2.0 ** -53)

@@ -6,10 +6,11 @@ The kernels live in csrc/ and build into _build/libfr_gb300.so (build.py).
 This Python layer only marshals arguments (ops.py over ctypes, _abi.py).
 """
 from ._abi import FrError, FrRopeParams, library_path, load
-from .ops import (decode_attn, decode_attn_noalloc, decode_attn_plan, kv_append, make_workspace, qkv_post,
+from .ops import (decode_attn, decode_attn_noalloc, decode_attn_noalloc_check, decode_attn_plan, kv_append, make_workspace, qkv_post,
                   rope_params,
                   workspace_check, workspace_size)
 
 __all__ = ["FrError", "FrRopeParams", "library_path", "load", "decode_attn", "decode_attn_noalloc",
+           "decode_attn_noalloc_check",
            "decode_attn_plan", "kv_append", "make_workspace",
            "qkv_post", "rope_params", "workspace_check", "workspace_size"]

@@ -57,6 +57,7 @@ SIGNATURES = {
     "fr_decode_attn": (_I, _ATTN_ARGS + [_P]),
     "fr_decode_attn_ex": (_I, _ATTN_ARGS + [ctypes.POINTER(FrAttnOpts), _P]),
     "fr_decode_attn_noalloc": (_I, _ATTN_ARGS[:18] + [_P]),
+    "fr_decode_attn_noalloc_check": (_I, [_P]),
     "fr_kv_append": (_I, [_P, _I64, _P, _I64, _P, _I, _I, _RP, _P, _I64, _P, _I64, _I64, _I64, _I64, _I64,
                           _P, _P, _P]),
     "fr_decode_attn_plan": (_I, [_I, _I, _I, _I, _I, _SZ, ctypes.POINTER(FrAttnOpts),

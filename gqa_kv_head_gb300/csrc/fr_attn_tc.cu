@@ -26,10 +26,10 @@
 //              O += P_hi,j V_j + P_lo,j V_j (A operand from TMEM, V read
 //              MN-major), commits.
 // Splits of one row tile form thread-block clusters of C CTAs (cluster dim y):
-//   prologue   each CTA multicasts its 1/C slice of the f16 Q rows by TMA. In
-//              the fused call the rows come from the qkv_post kernel launched
-//              just before (programmatic dependent launch: this kernel's set-up
-//              and first K/V loads overlap it).
+//   prologue   each CTA loads the whole 128-row f16 Q tile by TMA on its own
+//              (the rows sit in L2). In the fused call they come from the
+//              qkv_post kernel launched just before (programmatic dependent
+//              launch: this kernel's set-up and first K/V loads overlap it).
 //   epilogue   each CTA stores its (m, l, O) rows straight from TMEM into the
 //              shared memory of the CTA that owns them (rank c owns rows
 //              [c*128/C, (c+1)*128/C)); owners merge the C states locally, in
@@ -210,7 +210,6 @@ attn_tc_kernel(const __grid_constant__ TcArgs a, const __grid_constant__ Maps mp
     auto sMask = [&](int s) { return sStage + C::M_OFF + s * C::MASK_BYTES; };
 
     // ---- set-up ------------------------------------------------------------
-    const int my_r0 = (int)rank * R;
     if (tid == 0) {
         for (int s = 0; s < C::KS; ++s) {
             mbar_init(bar(C::B_KFULL + s), 1);
@@ -233,7 +232,7 @@ attn_tc_kernel(const __grid_constant__ TcArgs a, const __grid_constant__ Maps mp
         mbar_init(bar(C::B_PROBE), 1);
         mbar_init(bar(C::B_MMADONE), 1);
         mbar_fence_init();
-        // the whole Q tile arrives by TMA (each CTA multicasts its slice)
+        // the whole Q tile arrives by TMA (each CTA loads it on its own)
         mbar_expect_tx(bar(C::B_QFULL), (uint32_t)C::Q_BYTES);
         prefetch_tmap(&mp.k);
         prefetch_tmap(&mp.v);
@@ -290,18 +289,14 @@ attn_tc_kernel(const __grid_constant__ TcArgs a, const __grid_constant__ Maps mp
     }
 
     // ---- prologue: the 128 Q rows as f16, SW128 K-major in every CTA --------
-    // CTA rank c multicasts rows [c*R, (c+1)*R) to the cluster. When the rows
-    // come from the qkv_post grid launched just before this one (programmatic
-    // dependent launch), wait for that grid here: everything above overlapped it.
+    // Every CTA of a cluster loads the whole tile itself (the rows are in L2:
+    // qkv_post has just written them). When the rows come from the qkv_post
+    // grid launched just before this one (programmatic dependent launch), wait
+    // for that grid here: everything above overlapped it.
     if (tid == 0) {
         asm volatile("griddepcontrol.wait;" ::: "memory");
-        for (int b = 0; b < C::NB; ++b) {
-            const uint32_t dst = smem_addr(sQ + b * C::Q_BOX + my_r0 * 128);
-            if (CS == 1)
-                tma_load_2d(dst, &mp.q16, b * 64, row0 + my_r0, bar(C::B_QFULL));
-            else
-                tma_load_2d_mc(dst, &mp.q16, b * 64, row0 + my_r0, bar(C::B_QFULL), (uint16_t)((1u << CS) - 1u));
-        }
+        for (int b = 0; b < C::NB; ++b)
+            tma_load_2d(smem_addr(sQ + b * C::Q_BOX), &mp.q16, b * 64, row0, bar(C::B_QFULL));
     }
 
     if (a.probe_iters && tid == 0) {
@@ -358,8 +353,8 @@ attn_tc_kernel(const __grid_constant__ TcArgs a, const __grid_constant__ Maps mp
         }
     } else if (warp == kMmaWarp) {
         if (lane == 0) {
-            // the Q tile must have landed (full limit: other CTAs' multicasts
-            // write this CTA's shared memory)
+            // the Q tile must have landed (full limit: the copy writes this
+            // CTA's shared memory)
             if (!mbar_wait(bar(C::B_QFULL), 0, limit)) record_timeout(a.status, 1u);
             tc_fence_after();
             constexpr uint32_t idS = idesc_f16_f32(kRows, BN, 0, 0);
@@ -1026,7 +1021,7 @@ static fr_status launch(const TcLaunch& L, cudaStream_t stream) {
     if (a.has_mask &&
         !encode_2d(&mp.mask, L.mask, a.n_kv, a.n_tok, L.m_rs, 64, (uint32_t)(a.n_tok < kMaskWin ? a.n_tok : kMaskWin)))
         return FR_ERR_CUDA;
-    if (!a.q16 || !encode_2d(&mp.q16, a.q16, HD, a.M, HD, 64, kRows / a.C)) return FR_ERR_CUDA;
+    if (!a.q16 || !encode_2d(&mp.q16, a.q16, HD, a.M, HD, 64, kRows)) return FR_ERR_CUDA;
     if (a.merge_kernel &&
         !encode_2d_f32(&mp.po, a.part_o, HD, (uint64_t)L.row_tiles * a.splits * kRows, kOutBoxRows))
         return FR_ERR_CUDA;

@@ -6,6 +6,7 @@
 
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
+#include <math.h>
 #include <stdint.h>
 
 #include "fr_kernels.h"
@@ -114,6 +115,24 @@ __device__ __forceinline__ void rope_slot(const float* __restrict__ qrow, int c,
 }
 
 inline bool aligned16(const void* p) { return (((uintptr_t)p) & 15u) == 0; }
+
+// Host: p is device memory of GPU `dev` (or managed memory). A host pointer,
+// an unregistered address or memory of another GPU fails, before any launch.
+inline bool device_ptr_ok(const void* p, int dev) {
+    cudaPointerAttributes at;
+    if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+        (void)cudaGetLastError();          // reset the last-error state this call set
+        return false;
+    }
+    if (at.type == cudaMemoryTypeManaged) return true;
+    return at.type == cudaMemoryTypeDevice && at.device == dev;
+}
+
+// Host: the Q scale a call applies; FR_Q_SCALE_DEFAULT (0) selects 1/sqrt(hd)
+// (a zero scale has no use: it would make every score equal).
+inline float resolve_q_scale(float q_scale, int hd) {
+    return q_scale == 0.0f ? (float)(1.0 / sqrt((double)hd)) : q_scale;
+}
 
 // ---- PTX wrappers ---------------------------------------------------------
 

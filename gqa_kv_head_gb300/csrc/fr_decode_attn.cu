@@ -552,13 +552,18 @@ static fr_status decode_attn_impl(const uint16_t* q16, const float* q, int64_t q
         if (!q || !pos || !rp) return FR_ERR_INVALID_ARG;
         if (!aligned16(q) || q_tok_stride < (int64_t)n_head * hd || (q_tok_stride & 3))
             return FR_ERR_INVALID_ARG;
-        if (!build_rope_table(rp, q_scale, hd, &tb)) return FR_ERR_INVALID_ARG;
+        if (!build_rope_table(rp, resolve_q_scale(q_scale, hd), hd, &tb)) return FR_ERR_INVALID_ARG;
     }
     const int M = n_tok * n_head;
     if (ws_bytes < workspace_bytes_for(n_tok, n_head, hd, n_kv)) return FR_ERR_WORKSPACE;
 
     int dev = 0, sms = 152;
     if (cudaGetDevice(&dev) != cudaSuccess) return FR_ERR_CUDA;
+    // every buffer must be memory of the current GPU (not host memory, not a peer's)
+    if (!device_ptr_ok(k, dev) || !device_ptr_ok(v, dev) || !device_ptr_ok(out, dev) || !device_ptr_ok(ws, dev) ||
+        (mask && !device_ptr_ok(mask, dev)) || (q16 && !device_ptr_ok(q16, dev)) ||
+        (!q16 && (!device_ptr_ok(q, dev) || !device_ptr_ok(pos, dev))))
+        return FR_ERR_INVALID_ARG;
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return FR_ERR_CUDA;
     unsigned char* w = static_cast<unsigned char*>(ws);
 

@@ -21,7 +21,8 @@
 namespace {
 
 constexpr size_t kScratchBytes = (size_t)9 << 20;   // 9 MiB
-constexpr size_t kClearBytes = 1024;                 // status word + arrival tickets
+constexpr size_t kTicketsBegin = 256;                // arrival tickets: [256, 1024)
+constexpr size_t kTicketsEnd = 1024;                 // (the status word at [0, 4) is kept)
 constexpr int kMaxDevices = 64;
 
 // Scratch for the split-KV partial states, the arrival tickets and the status
@@ -63,9 +64,22 @@ extern "C" fr_status fr_decode_attn_noalloc(const uint16_t* q16, const float* q,
     void* ws = nullptr;
     const fr_status st = scratch_address(dev, &ws);
     if (st != FR_OK) return st;
-    // The array keeps whatever the previous call left: the status word and the
-    // arrival tickets must start at zero.
-    if (cudaMemsetAsync(ws, 0, kClearBytes, stream) != cudaSuccess) return FR_ERR_CUDA;
+    // The array keeps whatever the previous call left: the arrival tickets must
+    // start at zero. The status word is left alone, so that a device-side
+    // timeout stays visible until fr_decode_attn_noalloc_check reads it.
+    if (cudaMemsetAsync(static_cast<unsigned char*>(ws) + kTicketsBegin, 0, kTicketsEnd - kTicketsBegin, stream) !=
+        cudaSuccess)
+        return FR_ERR_CUDA;
     return fr_decode_attn(q16, q, q_tok_stride, pos, rp, q_scale, k, k_row_stride, v, v_row_stride, mask,
                           mask_row_stride, n_tok, n_head, hd, n_kv, kq_scale, out, ws, kScratchBytes, stream);
+}
+
+extern "C" fr_status fr_decode_attn_noalloc_check(cudaStream_t stream) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return FR_ERR_CUDA;
+    if (dev < 0 || dev >= kMaxDevices) return FR_ERR_UNSUPPORTED;
+    void* ws = nullptr;
+    const fr_status st = scratch_address(dev, &ws);
+    if (st != FR_OK) return st;
+    return fr_workspace_check(ws, stream);
 }

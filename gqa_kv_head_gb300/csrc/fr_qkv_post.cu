@@ -253,6 +253,12 @@ extern "C" fr_status fr_kv_append(const float* k_new, int64_t k_stride, const fl
     if (pad_end > pad_begin && pad_begin < row0 + n_tok && row0 < pad_end) return FR_ERR_INVALID_ARG;
     RopeTable tb;
     if (!build_rope_table(rp, 1.0f, hd, &tb)) return FR_ERR_INVALID_ARG;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return FR_ERR_CUDA;
+    if (!device_ptr_ok(k_new, dev) || !device_ptr_ok(v_new, dev) || !device_ptr_ok(pos, dev) ||
+        !device_ptr_ok(k_cache, dev) || !device_ptr_ok(v_cache, dev) || (k32_out && !device_ptr_ok(k32_out, dev)) ||
+        (v32_out && !device_ptr_ok(v32_out, dev)))
+        return FR_ERR_INVALID_ARG;
     const int64_t total = (int64_t)n_tok * (hd / 2) + ((int64_t)n_tok + (pad_end - pad_begin)) * (hd / 8);
     const int blocks = (int)(total < 256 * 1184 ? (total + 255) / 256 : 1184);
     cudaLaunchConfig_t cfg;
@@ -306,6 +312,11 @@ extern "C" fr_status fr_qkv_post(const float* q, int64_t q_tok_stride, const int
     if (!aligned16(q) || !aligned16(q16_out) || (q32_out && !aligned16(q32_out)))
         return FR_ERR_INVALID_ARG;
     RopeTable tb;
-    if (!build_rope_table(rp, q_scale, hd, &tb)) return FR_ERR_INVALID_ARG;
+    if (!build_rope_table(rp, resolve_q_scale(q_scale, hd), hd, &tb)) return FR_ERR_INVALID_ARG;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return FR_ERR_CUDA;
+    if (!device_ptr_ok(q, dev) || !device_ptr_ok(pos, dev) || !device_ptr_ok(q16_out, dev) ||
+        (q32_out && !device_ptr_ok(q32_out, dev)))
+        return FR_ERR_INVALID_ARG;
     return launch_qkv_post(q, q_tok_stride, pos, n_tok, n_head, hd, tb, q16_out, q32_out, stream);
 }

@@ -1,7 +1,6 @@
 // fr_sm100.cuh -- inline-PTX wrappers for the Blackwell (sm_100 family,
 // compiled for sm_103a) features the tensor-core attention kernel uses:
-// mbarriers with bounded waits, TMA tensor loads (optionally multicast within
-// a cluster), tcgen05 MMA / commit / TMEM load-store / alloc, shared-memory
+// mbarriers with bounded waits, TMA tensor loads and stores, tcgen05 MMA / commit / TMEM load-store / alloc, shared-memory
 // matrix descriptors, and cluster (DSMEM) addressing and barriers.
 #pragma once
 
@@ -73,22 +72,6 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
     asm volatile(
         "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
         :: "r"(dst), "l"((uint64_t)map), "r"(x), "r"(y), "r"(bar) : "memory");
-}
-// Same tile into the same shared-memory offset of every CTA in cta_mask; each
-// receiving CTA's barrier at offset `bar` is credited with the bytes.
-__device__ __forceinline__ void tma_load_2d_mc(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t bar,
-                                               uint16_t cta_mask) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster"
-        " [%0], [%1, {%2, %3}], [%4], %5;"
-        :: "r"(dst), "l"((uint64_t)map), "r"(x), "r"(y), "r"(bar), "h"(cta_mask) : "memory");
-}
-// Bulk copy of `bytes` (multiple of 16) from this CTA's shared memory to the
-// shared memory of a CTA in the cluster (dst and bar are shared::cluster
-// addresses from map_rank); the receiver's barrier is credited with the bytes.
-__device__ __forceinline__ void bulk_copy_to_peer(uint32_t dst, uint32_t src, uint32_t bytes, uint32_t bar) {
-    asm volatile("cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
-                 :: "r"(dst), "r"(src), "r"(bytes), "r"(bar) : "memory");
 }
 // TMA tensor store of one 2-D box from this CTA's shared memory (bulk-group
 // completion). x * element size must be a multiple of 16 bytes; x, y >= 0.

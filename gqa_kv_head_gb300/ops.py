@@ -5,7 +5,6 @@ and the current CUDA stream to the library, and raises FrError on a non-OK
 status. All arithmetic happens in the library's kernels.
 """
 import ctypes
-import math
 
 import torch
 
@@ -29,6 +28,11 @@ def _as_rope(rp):
 def _stream(stream):
     s = stream if stream is not None else torch.cuda.current_stream()
     return ctypes.c_void_p(s.cuda_stream)
+
+
+def _q_scale(q_scale):
+    """None -> FR_Q_SCALE_DEFAULT (0): the library applies 1/sqrt(hd)."""
+    return 0.0 if q_scale is None else float(q_scale)
 
 
 def _ptr(t):
@@ -59,13 +63,11 @@ def qkv_post(q, pos, n_head, hd, rope, q_scale=None, q16_out=None, q32_out=None,
     lib = _abi.load()
     _check_dev(q, pos, q16_out, q32_out)
     n_tok = q.shape[0]
-    if q_scale is None:
-        q_scale = 1.0 / math.sqrt(hd)
     if q16_out is None:
         q16_out = torch.empty((n_tok * n_head, hd), dtype=torch.float16, device=q.device)
     rp = _as_rope(rope)
     st = lib.fr_qkv_post(_ptr(q), _q_tok_stride(q, n_head, hd), _ptr(pos), n_tok, n_head, hd,
-                         ctypes.byref(rp), float(q_scale), _ptr(q16_out), _ptr(q32_out),
+                         ctypes.byref(rp), _q_scale(q_scale), _ptr(q16_out), _ptr(q32_out),
                          _stream(stream))
     _abi.check(st, "fr_qkv_post")
     return q16_out, q32_out
@@ -146,10 +148,8 @@ def decode_attn(k, v, n_tok, n_head, *, q16=None, q=None, pos=None, rope=None, q
             raise ValueError("pass q16, or q + pos + rope for the fused path")
         q_stride = _q_tok_stride(q, n_head, hd)
         rp = _as_rope(rope)
-        if q_scale is None:
-            q_scale = 1.0 / math.sqrt(hd)
     args = [_ptr(q16), _ptr(q), q_stride, _ptr(pos), ctypes.byref(rp) if rp is not None else None,
-            float(q_scale or 0.0), _ptr(k), _row_stride(k, "k"), _ptr(v), _row_stride(v, "v"),
+            _q_scale(q_scale), _ptr(k), _row_stride(k, "k"), _ptr(v), _row_stride(v, "v"),
             _ptr(mask), 0 if mask is None else _row_stride(mask, "mask"), n_tok, n_head, hd, n_kv,
             float(kq_scale), _ptr(out), _ptr(workspace), workspace.numel()]
     if splits is None and cluster is None and engine is None and not wait_probe_iters and not merge_mode:
@@ -197,12 +197,16 @@ def decode_attn_noalloc(k, v, n_tok, n_head, *, q16=None, q=None, pos=None, rope
             raise ValueError("pass q16, or q + pos + rope for the fused path")
         q_stride = _q_tok_stride(q, n_head, hd)
         rp = _as_rope(rope)
-        if q_scale is None:
-            q_scale = 1.0 / math.sqrt(hd)
     st = lib.fr_decode_attn_noalloc(
         _ptr(q16), _ptr(q), q_stride, _ptr(pos), ctypes.byref(rp) if rp is not None else None,
-        float(q_scale or 0.0), _ptr(k), _row_stride(k, "k"), _ptr(v), _row_stride(v, "v"), _ptr(mask),
+        _q_scale(q_scale), _ptr(k), _row_stride(k, "k"), _ptr(v), _row_stride(v, "v"), _ptr(mask),
         0 if mask is None else _row_stride(mask, "mask"), n_tok, n_head, hd, n_kv, float(kq_scale),
         _ptr(out), _stream(stream))
     _abi.check(st, "fr_decode_attn_noalloc")
     return out
+
+
+def decode_attn_noalloc_check(stream=None):
+    """fr_decode_attn_noalloc_check: raise FrError (FR_ERR_DEVICE_TIMEOUT) if a
+    bounded device-side wait of an earlier decode_attn_noalloc call gave up."""
+    _abi.check(_abi.load().fr_decode_attn_noalloc_check(_stream(stream)), "fr_decode_attn_noalloc_check")

@@ -24,14 +24,19 @@
  *    specialisations at the launch boundary.
  *
  * Conventions for every entry point
- *  - Device pointers unless stated otherwise; f16 tensors are IEEE binary16
- *    stored as uint16_t. Every pointer and every row stride (in bytes) must be
- *    16-byte aligned.
+ *  - Device pointers unless stated otherwise: memory of the GPU that is
+ *    current when the call is made (cudaMalloc'd or managed). Host memory and
+ *    another GPU's memory are rejected with FR_ERR_INVALID_ARG before any
+ *    launch; the library is for calls on one GPU. f16 tensors are IEEE
+ *    binary16 stored as uint16_t. Every pointer and every row stride (in
+ *    bytes) must be 16-byte aligned.
  *  - Row index r = t*n_head + h ("t-major"): Q16 rows and output rows.
  *  - Ownership: the caller owns every buffer. The library keeps no pointer
  *    after a call returns, never allocates or frees device memory and holds no
  *    mutable global state, so calls may be captured in a CUDA graph and made
  *    from several host threads (each concurrent call needs its own workspace).
+ *    The one exception is fr_decode_attn_noalloc (end of this file): its
+ *    calls share a scratch array inside the library and must not overlap.
  *  - Errors: arguments are validated on the host before any launch; an invalid
  *    call returns a status != FR_OK and launches nothing. A failed launch
  *    returns FR_ERR_CUDA. Nothing prints or aborts.
@@ -76,6 +81,10 @@ typedef struct fr_rope_params {
     int   n_ctx_orig;    /* > 0 when ext_factor != 0 */
 } fr_rope_params;
 
+/* Pass as q_scale to apply 1/sqrt(hd), the attention's usual scale (a zero
+ * scale has no use: it would make every score equal). */
+#define FR_Q_SCALE_DEFAULT 0.0f
+
 /* Human-readable name of a status code (static storage). */
 const char* fr_status_string(fr_status s);
 
@@ -92,7 +101,8 @@ int fr_abi_version(void);
  *            a multiple of 4 elements)
  *   pos      int32 [n_tok] token positions (shared by all heads of a token)
  *   rp       RoPE parameters (host pointer, read during the call only)
- *   q_scale  multiplier applied after the rotation (normally 1/sqrt(hd))
+ *   q_scale  multiplier applied after the rotation; FR_Q_SCALE_DEFAULT (0)
+ *            selects 1/sqrt(hd), rounded once to fp32
  *   q16_out  f16 [n_tok*n_head][hd], row r = t*n_head + h, contiguous
  *   q32_out  nullable; f32, same layout, the values q16_out is rounded from
  *
@@ -262,9 +272,11 @@ fr_status fr_decode_attn_plan(int n_tok, int n_head, int hd, int n_kv, int fused
  * n_tok*n_head > 256, return FR_ERR_WORKSPACE. No device memory is allocated.
  * The first call on each device looks up the array's device address
  * (cudaGetSymbolAddress); make that first call before any stream capture. Each
- * call clears the array's status word and arrival tickets on `stream` before
- * launching. Every call shares the one array: calls that overlap on the GPU
- * (other streams, other host threads) race and must be serialised by the caller.
+ * call clears the array's arrival tickets on `stream` before launching; its
+ * status word is kept, so a bounded device-side wait that gave up in any call
+ * is reported by the next fr_decode_attn_noalloc_check. Every call shares the
+ * one array: calls that overlap on the GPU (other streams, other host threads)
+ * race and must be serialised by the caller.
  */
 fr_status fr_decode_attn_noalloc(const uint16_t* q16,
                                  const float* q, int64_t q_tok_stride, const int32_t* pos,
@@ -274,6 +286,15 @@ fr_status fr_decode_attn_noalloc(const uint16_t* q16,
                                  const uint16_t* mask, int64_t mask_row_stride,
                                  int n_tok, int n_head, int hd, int n_kv, float kq_scale,
                                  float* out, cudaStream_t stream);
+
+/*
+ * fr_decode_attn_noalloc_check -- fr_workspace_check for the scratch array of
+ * fr_decode_attn_noalloc on the current device: synchronises `stream`, returns
+ * FR_ERR_DEVICE_TIMEOUT (and clears the word) if a bounded device-side wait of
+ * an earlier fr_decode_attn_noalloc call gave up, else FR_OK. Allocates
+ * nothing. The pages have no counterpart to this entry point.
+ */
+fr_status fr_decode_attn_noalloc_check(cudaStream_t stream);
 
 #ifdef __cplusplus
 }
