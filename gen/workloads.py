@@ -25,7 +25,10 @@ from .rng import normal, uniform
 
 @dataclass(frozen=True)
 class RopeParams:
-    """NEOX RoPE parameters with the YaRN terms, as ggml's rope_ext takes them."""
+    """NEOX RoPE parameters with the YaRN terms, as ggml's rope_ext takes them.
+    mode 0: angles exact modulo one turn; mode 1: ggml's fp32 angle evaluation.
+    freq_factors: None, or n_dims/2 per-pair divisors of the angle (rope_ext's
+    optional freq_factors input)."""
     n_dims: int
     freq_base: float = 10000.0
     freq_scale: float = 1.0
@@ -34,6 +37,8 @@ class RopeParams:
     beta_fast: float = 32.0
     beta_slow: float = 1.0
     n_ctx_orig: int = 4096
+    mode: int = 0
+    freq_factors: tuple = None
 
 
 @dataclass

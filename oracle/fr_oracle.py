@@ -59,10 +59,21 @@ def yarn_corr_dims(n_dims, n_ctx_orig, freq_base, beta_fast, beta_slow):
     return c0, c1
 
 
+def _freq_factors(rp):
+    """rope_ext's optional per-pair divisors of the angle (1 when absent)."""
+    half = rp.n_dims // 2
+    ff = getattr(rp, "freq_factors", None)
+    if ff is None:
+        return np.ones(half)
+    ff = np.asarray(ff, dtype=np.float64)
+    assert ff.shape == (half,)
+    return ff
+
+
 def rope_theta(pos, rp):
     """Angles theta[t, i] for pairs i < n_dims/2 and the magnitude factor mscale.
 
-    theta_ext = pos * base^(-2i/n_dims); theta_int = freq_scale * theta_ext.
+    theta_ext = pos * base^(-2i/n_dims) / ff_i; theta_int = freq_scale * theta_ext.
     With ext_factor != 0 the two are mixed by ramp(i) * ext_factor, where
     ramp(i) = 1 - clamp((i - c0) / max(0.001, c1 - c0), 0, 1), and mscale is
     attn_factor * (1 + 0.1 ln(1/freq_scale)); otherwise theta = theta_int and
@@ -71,7 +82,7 @@ def rope_theta(pos, rp):
     half = rp.n_dims // 2
     i = np.arange(half, dtype=np.float64)
     pos = np.asarray(pos, dtype=np.float64).reshape(-1, 1)
-    theta_ext = pos * np.power(float(rp.freq_base), -2.0 * i / rp.n_dims)
+    theta_ext = pos * np.power(float(rp.freq_base), -2.0 * i / rp.n_dims) / _freq_factors(rp)
     theta_int = float(rp.freq_scale) * theta_ext
     mscale = float(rp.attn_factor)
     if rp.ext_factor != 0.0:
@@ -87,10 +98,65 @@ def rope_theta(pos, rp):
     return theta, mscale
 
 
+def rope_theta_scale_f32(rp):
+    """ggml's fp32 ratio between consecutive pairs' angles: base raised to the
+    fp32 exponent fl(-2/n_dims), rounded once to fp32 (the correctly rounded
+    powf; computed here in double, then rounded)."""
+    e = np.float32(-2.0) / np.float32(rp.n_dims)
+    return np.float32(math.pow(float(np.float32(rp.freq_base)), float(e)))
+
+
+def rope_theta_f32(pos, rp):
+    """Angles of ggml's fp32 RoPE evaluation (mode 1) and its fp32 mscale.
+
+    Every step is one IEEE fp32 operation, rounded to nearest, in the order
+    ggml's rope cache takes them (no fused multiply-add):
+      theta_0 = fl(pos); theta_i = fl(theta_{i-1} * theta_scale)
+      theta_ext = fl(theta_i / ff_i); theta_int = fl(freq_scale * theta_ext)
+      ext_factor != 0:  y = fl(fl(i - c0) / max(0.001, fl(c1 - c0)))
+                        ramp_mix = fl(fl(1 - clamp(y, 0, 1)) * ext_factor)
+                        theta = fl(fl(theta_int * fl(1 - ramp_mix)) + fl(theta_ext * ramp_mix))
+                        mscale = fl(attn_factor * fl(1 + fl(0.1 * fl(ln(fl(1 / freq_scale))))))
+      else:             theta = theta_int, mscale = attn_factor
+    The correction dims c0, c1 are the integers yarn_corr_dims gives. The
+    logarithm is rounded once to fp32 from double. Returns (theta float32
+    [n_tok, n_dims/2], mscale float32)."""
+    f32 = np.float32
+    half = rp.n_dims // 2
+    ts = rope_theta_scale_f32(rp)
+    pos = np.asarray(pos).reshape(-1)
+    theta = np.empty((pos.shape[0], half), dtype=f32)
+    cur = pos.astype(f32)
+    for i in range(half):
+        if i > 0:
+            cur = (cur * ts).astype(f32)
+        theta[:, i] = cur
+    ff = _freq_factors(rp).astype(f32)
+    th_ext = (theta / ff[None, :]).astype(f32)
+    th_int = (f32(rp.freq_scale) * th_ext).astype(f32)
+    mscale = f32(rp.attn_factor)
+    if rp.ext_factor != 0.0:
+        c0, c1 = yarn_corr_dims(rp.n_dims, rp.n_ctx_orig, rp.freq_base, rp.beta_fast, rp.beta_slow)
+        c0, c1 = f32(c0), f32(c1)
+        i = np.arange(half).astype(f32)
+        y = ((i - c0).astype(f32) / np.maximum(f32(0.001), f32(c1 - c0))).astype(f32)
+        ramp = (f32(1.0) - np.minimum(f32(1.0), np.maximum(f32(0.0), y))).astype(f32)
+        mix = (ramp * f32(rp.ext_factor)).astype(f32)
+        a = (th_int * (f32(1.0) - mix).astype(f32)[None, :]).astype(f32)
+        b = (th_ext * mix[None, :]).astype(f32)
+        th = (a + b).astype(f32)
+        lg = f32(math.log(float(f32(1.0) / f32(rp.freq_scale))))
+        mscale = f32(mscale * f32(f32(1.0) + f32(f32(0.1) * lg)))
+    else:
+        th = th_int
+    return th, mscale
+
+
 def rope_neox(x, pos, rp):
     """NEOX rotation of x [n_tok, n_head, hd] at positions pos [n_tok].
 
-    Pair i rotates (x[i], x[i + n_dims/2]) by theta[t, i], scaled by mscale:
+    Pair i rotates (x[i], x[i + n_dims/2]) by theta[t, i] (rope_theta, or
+    rope_theta_f32 when rp.mode == 1), scaled by mscale:
         y[i]          = x[i] * c - x[i + n/2] * s
         y[i + n/2]    = x[i] * s + x[i + n/2] * c,   c = mscale cos, s = mscale sin
     Dimensions >= n_dims pass through unchanged. Every head of token t uses the
@@ -99,7 +165,11 @@ def rope_neox(x, pos, rp):
     x = np.asarray(x, dtype=np.float64)
     n = rp.n_dims
     half = n // 2
-    theta, mscale = rope_theta(pos, rp)
+    if getattr(rp, "mode", 0) == 1:
+        th32, ms32 = rope_theta_f32(pos, rp)             # ggml's fp32 angles, cos/sin in fp64
+        theta, mscale = th32.astype(np.float64), float(ms32)
+    else:
+        theta, mscale = rope_theta(pos, rp)
     c = (mscale * np.cos(theta))[:, None, :]          # [n_tok, 1, half]
     s = (mscale * np.sin(theta))[:, None, :]
     y = x.copy()

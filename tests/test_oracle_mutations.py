@@ -33,6 +33,14 @@ MUTANTS = {
                             "k_rope = rope_neox(k_new[:, None, :], -np.asarray(pos), rp)[:, 0, :]"),
     "tail_off_by_one": ("kc[row0:row0 + n_tok] = f16_round(k_rope)", "kc[row0 + 1:row0 + 1 + n_tok] = f16_round(k_rope)"),
     "pad_not_zeroed": ("        kc[pad[0]:pad[1]] = 0\n", ""),
+    "f32_recurrence_off_by_one": ("        if i > 0:\n            cur = (cur * ts).astype(f32)\n",
+                                  "        cur = (cur * ts).astype(f32)\n"),
+    "f32_freq_factor_multiplied": ("th_ext = (theta / ff[None, :]).astype(f32)",
+                                   "th_ext = (theta * ff[None, :]).astype(f32)"),
+    "f32_mix_terms_swapped": ("a = (th_int * (f32(1.0) - mix)", "a = (th_ext * (f32(1.0) - mix)"),
+    "f32_mscale_dropped": ("mscale = f32(mscale * f32(f32(1.0) + f32(f32(0.1) * lg)))", "mscale = f32(mscale)"),
+    "f32_exponent_in_double": ("e = np.float32(-2.0) / np.float32(rp.n_dims)", "e = -2.0 / rp.n_dims + 1e-9"),
+    "freq_factors_ignored": ("-2.0 * i / rp.n_dims) / _freq_factors(rp)", "-2.0 * i / rp.n_dims)"),
 }
 
 
@@ -47,6 +55,7 @@ def test_pins_catch_mutant(name, tmp_path):
     r = subprocess.run([sys.executable, "-m", "pytest", "-q", "-x", "-p", "no:cacheprovider",
                         os.path.join(HERE, "test_oracle_rope.py"),
                         os.path.join(HERE, "test_oracle_attn.py"),
-                        os.path.join(HERE, "test_oracle_kv.py")],
+                        os.path.join(HERE, "test_oracle_kv.py"),
+                        os.path.join(HERE, "test_oracle_rope_f32.py")],
                        env=env, capture_output=True, text=True, cwd=os.path.dirname(HERE))
     assert r.returncode != 0, f"mutant {name} survived the oracle pins:\n{r.stdout[-2000:]}"
