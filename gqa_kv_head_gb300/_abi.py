@@ -19,11 +19,16 @@ class FrError(RuntimeError):
         super().__init__(f"{where}: {STATUS_NAMES.get(status, status)}")
 
 
+FR_ROPE_EXACT = 0
+FR_ROPE_GGML_F32 = 1
+
+
 class FrRopeParams(ctypes.Structure):
     _fields_ = [("n_dims", ctypes.c_int), ("freq_base", ctypes.c_float),
                 ("freq_scale", ctypes.c_float), ("ext_factor", ctypes.c_float),
                 ("attn_factor", ctypes.c_float), ("beta_fast", ctypes.c_float),
-                ("beta_slow", ctypes.c_float), ("n_ctx_orig", ctypes.c_int)]
+                ("beta_slow", ctypes.c_float), ("n_ctx_orig", ctypes.c_int),
+                ("mode", ctypes.c_int), ("freq_factors", ctypes.POINTER(ctypes.c_float))]
 
 
 class FrAttnOpts(ctypes.Structure):

@@ -31,17 +31,28 @@ inline bool decode_shape(int n_tok, int n_head) {
 }
 
 // Per-launch RoPE constants (kernel parameter, by value).
+// Mode FR_ROPE_EXACT:
 //   turns[i] = frac(w_i / 2pi) * 2^64, w_i = effective angle per position of
-//   pair i (base^(-2i/n_dims) times the YaRN interpolation factor). The angle
-//   of pair i at integer position p is then 2pi * ((p * turns[i]) mod 2^64) /
-//   2^64: the product wraps exactly modulo one turn, so large positions lose
-//   no precision to the range reduction.
+//   pair i (base^(-2i/n_dims) / ff_i times the YaRN interpolation factor). The
+//   angle of pair i at integer position p is then 2pi * ((p * turns[i]) mod
+//   2^64) / 2^64: the product wraps exactly modulo one turn, so large
+//   positions lose no precision to the range reduction.
+// Mode FR_ROPE_GGML_F32 (ggml's fp32 evaluation, one IEEE fp32 operation per
+// step): theta_0 = fl(p), theta_i = fl(theta_{i-1} * theta_scale); theta_ext =
+// fl(theta_i / ff_i); theta_int = fl(freq_scale * theta_ext); with YaRN,
+// theta = fl(fl(theta_int * fl(1 - mix_i)) + fl(theta_ext * mix_i)).
 struct RopeTable {
-    uint64_t turns[kMaxPairs];
+    uint64_t turns[kMaxPairs];   // exact mode
+    float mix[kMaxPairs];        // fp32 mode: fl(ramp_i * ext_factor)
+    float ff[kMaxPairs];         // fp32 mode: freq factor of pair i (1 when absent)
     float mscale;       // attn_factor (* (1 + 0.1 ln(1/freq_scale)) with YaRN)
     float q_scale;      // applied after the rotation
+    float theta_scale;  // fp32 mode: fl(base ^ fl(-2/n_dims))
+    float freq_scale;   // fp32 mode
     int half;           // n_dims / 2
     int n_dims;
+    int mode;           // FR_ROPE_EXACT or FR_ROPE_GGML_F32
+    int yarn;           // ext_factor != 0
 };
 
 // Host: validate the parameters and fill the table. Returns false if invalid.
@@ -55,13 +66,36 @@ fr_status launch_qkv_post(const float* q, int64_t q_tok_stride, const int32_t* p
 constexpr int kQkvThreads = 256;
 constexpr int kQkvHeads = 4;
 
-// Scaled cosine and sine of pair i at integer position pos.
+// Scaled cosine and sine of pair i at integer position pos (exact mode).
 __device__ __forceinline__ void rope_cs(int pos, uint64_t turns, float mscale, float& c, float& s) {
     const uint64_t a = (uint64_t)(int64_t)pos * turns;      // mod 2^64 = mod one turn
     const float half_turns = (float)(int64_t)a * 0x1p-63f;   // angle / pi in [-1, 1)
     sincospif(half_turns, &s, &c);
     c = __fmul_rn(c, mscale);
     s = __fmul_rn(s, mscale);
+}
+
+// Angle of pair i at position pos in ggml's fp32 evaluation (see RopeTable).
+__device__ __forceinline__ float rope_theta_f32(int pos, int i, const RopeTable& tb) {
+    float th = __int2float_rn(pos);
+    const float ts = tb.theta_scale;
+    for (int j = 0; j < i; ++j) th = __fmul_rn(th, ts);
+    const float te = __fdiv_rn(th, tb.ff[i]);
+    const float ti = __fmul_rn(tb.freq_scale, te);
+    if (!tb.yarn) return ti;
+    const float m = tb.mix[i];
+    return __fadd_rn(__fmul_rn(ti, __fsub_rn(1.0f, m)), __fmul_rn(te, m));
+}
+
+// Scaled cosine and sine of pair i at position pos, either mode.
+__device__ __forceinline__ void rope_cs_tab(int pos, int i, const RopeTable& tb, float& c, float& s) {
+    if (tb.mode == FR_ROPE_GGML_F32) {
+        sincosf(rope_theta_f32(pos, i, tb), &s, &c);
+        c = __fmul_rn(c, tb.mscale);
+        s = __fmul_rn(s, tb.mscale);
+    } else {
+        rope_cs(pos, tb.turns[i], tb.mscale, c, s);
+    }
 }
 
 // The two rotated outputs of a pair, from the scaled cos/sin. Plain IEEE fp32
@@ -74,15 +108,6 @@ __device__ __forceinline__ float rope_hi(float x0, float x1, float c, float s, f
     return __fmul_rn(__fmaf_rn(x0, s, __fmul_rn(x1, c)), q_scale);
 }
 
-// Rotate (x0, x1) of pair i at position pos, then scale.
-__device__ __forceinline__ void rope_pair(float x0, float x1, int pos, uint64_t turns,
-                                          float mscale, float q_scale,
-                                          float& y0, float& y1) {
-    float c, s;
-    rope_cs(pos, turns, mscale, c, s);
-    y0 = rope_lo(x0, x1, c, s, q_scale);
-    y1 = rope_hi(x0, x1, c, s, q_scale);
-}
 
 // One "slot" of a Q row: slot c < half rotates dims (c, c + half); slot
 // c >= half passes dims n_dims + 2(c - half) and +1 through (scaled).
@@ -101,7 +126,10 @@ __device__ __forceinline__ void rope_slot_dims(int c, const RopeTable& tb, int& 
 __device__ __forceinline__ void rope_slot_apply(int c, float x0, float x1, int pos, const RopeTable& tb,
                                                 float& y0, float& y1) {
     if (c < tb.half) {
-        rope_pair(x0, x1, pos, tb.turns[c], tb.mscale, tb.q_scale, y0, y1);
+        float cs, sn;
+        rope_cs_tab(pos, c, tb, cs, sn);
+        y0 = rope_lo(x0, x1, cs, sn, tb.q_scale);
+        y1 = rope_hi(x0, x1, cs, sn, tb.q_scale);
     } else {
         y0 = __fmul_rn(x0, tb.q_scale);
         y1 = __fmul_rn(x1, tb.q_scale);

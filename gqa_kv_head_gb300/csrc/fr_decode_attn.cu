@@ -157,10 +157,13 @@ attn_v1_kernel(const __grid_constant__ AttnArgs a, const __grid_constant__ RopeT
             const int p = __ldg(a.pos + t);
             int d0, d1;
             float y0, y1;
-            if (c < T.half) {
+            if (c < T.half && T.mode == FR_ROPE_EXACT) {
                 d0 = c;
                 d1 = c + T.half;
-                rope_pair(qrow[d0], qrow[d1], p, sTurns[c], T.mscale, T.q_scale, y0, y1);
+                float cs, sn;
+                rope_cs(p, sTurns[c], T.mscale, cs, sn);
+                y0 = rope_lo(qrow[d0], qrow[d1], cs, sn, T.q_scale);
+                y1 = rope_hi(qrow[d0], qrow[d1], cs, sn, T.q_scale);
             } else {
                 rope_slot(qrow, c, p, T, d0, d1, y0, y1);
             }

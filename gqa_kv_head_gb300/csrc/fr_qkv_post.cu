@@ -29,23 +29,61 @@ static void yarn_corr_dims(int n_dims, int n_ctx_orig, double base, double beta_
 
 bool build_rope_table(const fr_rope_params* rp, float q_scale, int hd, RopeTable* t) {
     if (!rp || !t) return false;
+    memset(t, 0, sizeof(*t));
     const int n = rp->n_dims;
     if (n < 2 || (n & 1) || n > hd || n / 2 > kMaxPairs) return false;
     if (!(rp->freq_base > 0.0f) || !(rp->freq_scale > 0.0f)) return false;
+    if (!isfinite(rp->freq_base) || !isfinite(rp->freq_scale)) return false;
     if (!isfinite(rp->ext_factor) || !isfinite(rp->attn_factor) || !isfinite(q_scale)) return false;
+    if (rp->mode != FR_ROPE_EXACT && rp->mode != FR_ROPE_GGML_F32) return false;
+    const int half = n / 2;
+    if (rp->freq_factors)
+        for (int i = 0; i < half; ++i)
+            if (!(rp->freq_factors[i] > 0.0f) || !isfinite(rp->freq_factors[i])) return false;
     const bool yarn = rp->ext_factor != 0.0f;
     double c0 = 0.0, c1 = 0.0;
     if (yarn) {
         if (rp->n_ctx_orig <= 0 || !(rp->beta_fast > 0.0f) || !(rp->beta_slow > 0.0f)) return false;
         yarn_corr_dims(n, rp->n_ctx_orig, rp->freq_base, rp->beta_fast, rp->beta_slow, &c0, &c1);
     }
+    t->half = half;
+    t->n_dims = n;
+    t->mode = rp->mode;
+    t->yarn = yarn ? 1 : 0;
+    t->q_scale = q_scale;
+    for (int i = 0; i < half; ++i) t->ff[i] = rp->freq_factors ? rp->freq_factors[i] : 1.0f;
+    if (rp->mode == FR_ROPE_GGML_F32) {
+        // one IEEE fp32 operation per step (the host objects are built with
+        // floating-point contraction off, so no step is fused); powf and logf
+        // are the correctly rounded values, taken in double and rounded once
+        const float e = -2.0f / (float)n;
+        t->theta_scale = (float)pow((double)rp->freq_base, (double)e);
+        t->freq_scale = rp->freq_scale;
+        const float lo = (float)c0, hi = (float)c1;
+        for (int i = 0; i < half; ++i) {
+            if (!yarn) {
+                t->mix[i] = 0.0f;
+                continue;
+            }
+            const float y = ((float)i - lo) / fmaxf(0.001f, hi - lo);
+            const float ramp = 1.0f - fminf(1.0f, fmaxf(0.0f, y));
+            t->mix[i] = ramp * rp->ext_factor;
+        }
+        float ms = rp->attn_factor;
+        if (yarn) {
+            const float lg = (float)log((double)(1.0f / rp->freq_scale));
+            const float f = 1.0f + 0.1f * lg;
+            ms = ms * f;
+        }
+        t->mscale = ms;
+        return true;
+    }
     const double two_pi = 6.283185307179586476925286766559;
     const double step = pow((double)rp->freq_base, -2.0 / n);   // ratio between pairs
     const double fs = rp->freq_scale;
-    double w_ext = 1.0;
-    t->half = n / 2;
-    t->n_dims = n;
-    for (int i = 0; i < t->half; ++i) {
+    double w_base = 1.0;
+    for (int i = 0; i < half; ++i) {
+        const double w_ext = w_base / (double)t->ff[i];
         double w = fs * w_ext;                                   // interpolation
         if (yarn) {
             const double y = ((double)i - c0) / fmax(0.001, c1 - c0);
@@ -57,14 +95,34 @@ bool build_rope_table(const fr_rope_params* rp, float q_scale, int hd, RopeTable
         f -= floor(f);                                           // turns per step, mod 1
         const double scaled = ldexp(f, 64);
         t->turns[i] = scaled >= 18446744073709551616.0 ? 0ull : (uint64_t)scaled;
-        w_ext *= step;
+        w_base *= step;
     }
-    for (int i = t->half; i < kMaxPairs; ++i) t->turns[i] = 0;
     double mscale = rp->attn_factor;
     if (yarn) mscale *= 1.0 + 0.1 * log(1.0 / fs);
     t->mscale = (float)mscale;
-    t->q_scale = q_scale;
     return true;
+}
+
+// The parameter table into shared memory (block-wide; ends with a barrier):
+// indexing the kernel-parameter copy with a per-thread slot would serialise
+// every access.
+__device__ __forceinline__ void copy_rope_table(const RopeTable& tb, RopeTable& stb, int pairs) {
+    for (int c = threadIdx.x; c < pairs; c += blockDim.x) {
+        stb.turns[c] = tb.turns[c];
+        stb.mix[c] = tb.mix[c];
+        stb.ff[c] = tb.ff[c];
+    }
+    if (threadIdx.x == 0) {
+        stb.mscale = tb.mscale;
+        stb.q_scale = tb.q_scale;
+        stb.theta_scale = tb.theta_scale;
+        stb.freq_scale = tb.freq_scale;
+        stb.half = tb.half;
+        stb.n_dims = tb.n_dims;
+        stb.mode = tb.mode;
+        stb.yarn = tb.yarn;
+    }
+    __syncthreads();
 }
 
 // Every query head of a token rotates its pairs by the same angles, so a work
@@ -82,17 +140,8 @@ qkv_post_kernel(const float* __restrict__ q, int64_t q_tok_stride, const int32_t
     // waits for this grid's completion before it reads the rows.
     asm volatile("griddepcontrol.wait;" ::: "memory");
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    // the table in shared memory: indexing the parameter copy with a
-    // per-thread slot would serialise every access
     __shared__ RopeTable stb;
-    for (int c = threadIdx.x; c < HD / 2; c += blockDim.x) stb.turns[c] = tb.turns[c];
-    if (threadIdx.x == 0) {
-        stb.mscale = tb.mscale;
-        stb.q_scale = tb.q_scale;
-        stb.half = tb.half;
-        stb.n_dims = tb.n_dims;
-    }
-    __syncthreads();
+    copy_rope_table(tb, stb, HD / 2);
     constexpr int SLOTS = HD / 2;
     const int groups = (n_head + kQkvHeads - 1) / kQkvHeads;
     const int64_t items = (int64_t)n_tok * groups * SLOTS;
@@ -113,7 +162,7 @@ qkv_post_kernel(const float* __restrict__ q, int64_t q_tok_stride, const int32_t
         }
         const bool rot = c < stb.half;
         float cs = 0.f, sn = 0.f;
-        if (rot) rope_cs(__ldg(pos + t), stb.turns[c], stb.mscale, cs, sn);
+        if (rot) rope_cs_tab(__ldg(pos + t), c, stb, cs, sn);
         const int64_t r0 = (int64_t)t * n_head + h0;       // t-major row of head h0
 #pragma unroll
         for (int u = 0; u < kQkvHeads; ++u) {
@@ -178,14 +227,7 @@ kv_append_kernel(const float* __restrict__ k_new, int64_t k_stride, const float*
     asm volatile("griddepcontrol.wait;" ::: "memory");
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     __shared__ RopeTable stb;                                  // see qkv_post_kernel
-    for (int i = threadIdx.x; i < kMaxPairs; i += blockDim.x) stb.turns[i] = tb.turns[i];
-    if (threadIdx.x == 0) {
-        stb.mscale = tb.mscale;
-        stb.q_scale = tb.q_scale;
-        stb.half = tb.half;
-        stb.n_dims = tb.n_dims;
-    }
-    __syncthreads();
+    copy_rope_table(tb, stb, HD / 2);
     constexpr int G = HD / 8;                                  // 8-element groups per row
     const int64_t nK = (int64_t)n_tok * (HD / 2), nV = (int64_t)n_tok * G, nP = pad_rows * G;
     for (int64_t w = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; w < nK + nV + nP;
@@ -298,7 +340,7 @@ extern "C" const char* fr_status_string(fr_status s) {
     return "unknown fr_status";
 }
 
-extern "C" int fr_abi_version(void) { return (1 << 16) | 0; }
+extern "C" int fr_abi_version(void) { return (2 << 16) | 0; }
 
 extern "C" fr_status fr_qkv_post(const float* q, int64_t q_tok_stride, const int32_t* pos,
                                  int n_tok, int n_head, int hd, const fr_rope_params* rp,

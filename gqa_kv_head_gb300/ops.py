@@ -13,16 +13,25 @@ from ._abi import FrAttnOpts, FrError, FrRopeParams
 
 
 def rope_params(n_dims, freq_base=10000.0, freq_scale=1.0, ext_factor=0.0, attn_factor=1.0,
-                beta_fast=32.0, beta_slow=1.0, n_ctx_orig=4096):
-    return FrRopeParams(int(n_dims), float(freq_base), float(freq_scale), float(ext_factor),
-                        float(attn_factor), float(beta_fast), float(beta_slow), int(n_ctx_orig))
+                beta_fast=32.0, beta_slow=1.0, n_ctx_orig=4096, mode=0, freq_factors=None):
+    """fr_rope_params. mode: 0 = FR_ROPE_EXACT, 1 = FR_ROPE_GGML_F32;
+    freq_factors: None or n_dims/2 floats (kept alive by the returned struct)."""
+    ff = None
+    if freq_factors is not None:
+        ff = (ctypes.c_float * len(freq_factors))(*[float(x) for x in freq_factors])
+    rp = FrRopeParams(int(n_dims), float(freq_base), float(freq_scale), float(ext_factor),
+                      float(attn_factor), float(beta_fast), float(beta_slow), int(n_ctx_orig), int(mode),
+                      ctypes.cast(ff, ctypes.POINTER(ctypes.c_float)) if ff is not None else None)
+    rp._ff_keepalive = ff
+    return rp
 
 
 def _as_rope(rp):
     if rp is None or isinstance(rp, FrRopeParams):
         return rp
     return rope_params(rp.n_dims, rp.freq_base, rp.freq_scale, rp.ext_factor, rp.attn_factor,
-                       rp.beta_fast, rp.beta_slow, rp.n_ctx_orig)
+                       rp.beta_fast, rp.beta_slow, rp.n_ctx_orig, getattr(rp, "mode", 0),
+                       getattr(rp, "freq_factors", None))
 
 
 def _stream(stream):

@@ -63,13 +63,32 @@ typedef enum fr_status {
 } fr_status;
 
 /* RoPE parameters, NEOX mode, with the YaRN terms as ggml's rope_ext takes
- * them (FlashRT-llama.cpp development guide, "Invariants and pitfalls").
+ * them (FlashRT-llama.cpp development guide, "Invariants and pitfalls": RoPE
+ * mirrors ggml's rope_neox, YaRN corrections included).
  * Pair i < n_dims/2 rotates (x[i], x[i + n_dims/2]); dims >= n_dims pass
- * through. theta_ext = pos * freq_base^(-2i/n_dims), theta_int = freq_scale *
- * theta_ext; with ext_factor != 0 they are mixed by the YaRN ramp between the
- * correction dims of beta_fast/beta_slow (n_ctx_orig) and the magnitude is
- * attn_factor * (1 + 0.1 ln(1/freq_scale)); otherwise theta = theta_int and
- * the magnitude is attn_factor. */
+ * through. theta_ext = pos * freq_base^(-2i/n_dims) / ff_i, theta_int =
+ * freq_scale * theta_ext; with ext_factor != 0 they are mixed by the YaRN ramp
+ * between the correction dims of beta_fast/beta_slow (n_ctx_orig) and the
+ * magnitude is attn_factor * (1 + 0.1 ln(1/freq_scale)); otherwise theta =
+ * theta_int and the magnitude is attn_factor.
+ *
+ * mode selects how the angles are evaluated:
+ *   FR_ROPE_EXACT     pos * w_i reduced exactly modulo one turn (64-bit fixed
+ *                     point; w_i from double on the host), sincospi in fp32.
+ *   FR_ROPE_GGML_F32  ggml's fp32 evaluation, one IEEE fp32 operation per step
+ *                     in ggml's order: theta_scale = fl(freq_base ^ fl(-2/n_dims))
+ *                     (correctly rounded), theta_0 = fl(pos), theta_i =
+ *                     fl(theta_{i-1} * theta_scale), theta_ext = fl(theta_i / ff_i),
+ *                     theta_int = fl(freq_scale * theta_ext), YaRN mix
+ *                     fl(fl(theta_int * fl(1 - m_i)) + fl(theta_ext * m_i)) with
+ *                     m_i = fl(ramp_i * ext_factor); then fp32 sincos and the
+ *                     fp32 magnitude fl(attn_factor * fl(1 + fl(0.1 * ln(1/freq_scale)))).
+ *                     The angles are bit-exact with that recurrence; at large
+ *                     positions they carry its fp32 error (~1e-7 relative per step).
+ * freq_factors: nullable host pointer to n_dims/2 floats (finite, > 0), the
+ * per-pair divisors ff_i of rope_ext (1 when NULL); read during the call only. */
+#define FR_ROPE_EXACT 0
+#define FR_ROPE_GGML_F32 1
 typedef struct fr_rope_params {
     int   n_dims;        /* rotated dims: even, 2 <= n_dims <= hd */
     float freq_base;     /* > 0 */
@@ -79,6 +98,8 @@ typedef struct fr_rope_params {
     float beta_fast;
     float beta_slow;
     int   n_ctx_orig;    /* > 0 when ext_factor != 0 */
+    int   mode;          /* FR_ROPE_EXACT or FR_ROPE_GGML_F32 */
+    const float* freq_factors;   /* nullable, n_dims/2 host floats */
 } fr_rope_params;
 
 /* Pass as q_scale to apply 1/sqrt(hd), the attention's usual scale (a zero
@@ -106,8 +127,8 @@ int fr_abi_version(void);
  *   q16_out  f16 [n_tok*n_head][hd], row r = t*n_head + h, contiguous
  *   q32_out  nullable; f32, same layout, the values q16_out is rounded from
  *
- * Arithmetic: angles reduced exactly modulo one turn (64-bit fixed point),
- * rotation and scale in fp32, one round-to-nearest to f16.
+ * Arithmetic: angles as rp->mode says (fr_rope_params), rotation and scale
+ * in fp32, one round-to-nearest to f16.
  * Supported: 1 <= n_tok <= 8192, 1 <= n_head, M = n_tok*n_head <= 65536,
  * hd in {64, 128, 256}.
  */

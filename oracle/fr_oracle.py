@@ -60,12 +60,14 @@ def yarn_corr_dims(n_dims, n_ctx_orig, freq_base, beta_fast, beta_slow):
 
 
 def _freq_factors(rp):
-    """rope_ext's optional per-pair divisors of the angle (1 when absent)."""
+    """rope_ext's optional per-pair divisors of the angle (1 when absent). They
+    are an fp32 input (ggml's rope_ext takes an F32 tensor), so they are
+    rounded to fp32 first, like the Q rows."""
     half = rp.n_dims // 2
     ff = getattr(rp, "freq_factors", None)
     if ff is None:
         return np.ones(half)
-    ff = np.asarray(ff, dtype=np.float64)
+    ff = np.asarray(ff, dtype=np.float32).astype(np.float64)
     assert ff.shape == (half,)
     return ff
 

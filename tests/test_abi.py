@@ -44,7 +44,7 @@ def test_status_strings_and_version(lib):
     assert lib.fr_status_string(0) == b"FR_OK"
     for s in range(1, 6):
         assert lib.fr_status_string(s).startswith(b"FR_ERR_")
-    assert lib.fr_abi_version() >> 16 == 1
+    assert lib.fr_abi_version() >> 16 == 2
 
 
 def test_workspace_size_host_logic(lib):
@@ -114,6 +114,9 @@ def test_qkv_post_validation(lib):
     assert call(rp=rope_params(256)) == 1            # n_dims > hd
     assert call(rp=rope_params(128, freq_base=-1.0)) == 1
     assert call(rp=rope_params(128, ext_factor=1.0, n_ctx_orig=0)) == 1
+    assert call(rp=rope_params(128, mode=2)) == 1                       # unknown angle mode
+    assert call(rp=rope_params(128, freq_factors=[1.0] * 63 + [0.0])) == 1   # a zero divisor
+    assert call(rp=rope_params(128, mode=1, freq_factors=[1.0] * 63 + [float("nan")])) == 1
 
 
 def test_plan_validation(lib):
