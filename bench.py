@@ -478,7 +478,8 @@ def run_ours(args, rank, world, local_rank):
                          f"{w.name} workload, ~{args.cpu_seconds:.0f} s"}
 
     plan = fr.decode_attn_plan(w.n_tok, w.n_head, w.hd, w.n_kv, workspace_bytes=ws.numel())
-    attn_kernels = "attn_tc_kernel + attn_merge_kernel" if plan["merge_kernel"] else "attn_tc_kernel"
+    main_kernel = "attn_sw_kernel" if plan.get("keys_on_m") else "attn_tc_kernel"
+    attn_kernels = f"{main_kernel} + attn_merge_kernel" if plan["merge_kernel"] else main_kernel
     peaks = load_peaks()
     peak = peaks["hbm_gbs"]
     attn_bytes = attention_bytes(w)

@@ -2,6 +2,7 @@
 // (validation, planning, workspace layout) and the tensor-core kernel.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_fp16.h>
 #include <stdint.h>
 
@@ -47,13 +48,60 @@ struct TcLaunch {
 };
 
 int tile_keys(int hd, int n_kv, int row_tiles, int num_sms);
+// 2-D f16 tensor map [rows][inner] (row stride in elements), 128-byte swizzle
+// or none.
+bool encode_f16_2d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows, uint64_t row_stride,
+                   uint32_t box_inner, uint32_t box_rows, bool swizzle128);
 fr_status launch_tc(const TcLaunch& L, int hd, cudaStream_t stream);
 // Merge of the split states written in merge-kernel mode (programmatic
 // dependent launch after the attention grid).
 fr_status launch_merge(const float* part_o, const float2* part_ml, float* out, int M, int splits, int hd,
-                       cudaStream_t stream);
+                       int rstride, cudaStream_t stream);
 
 }  // namespace tc
+
+// The kernel with the KV tile on the MMA's M side, for M <= 64 query rows
+// (fr_attn_sw.cu): one KV split per CTA.
+namespace sw {
+
+constexpr int kMaxRows = 64;
+
+struct SwArgs {
+    float* out;
+    float* part_o;            // [splits][rstride][hd] unnormalised O rows (splits > 1)
+    float2* part_ml;          // [splits][rstride] (row max in log2 units, row sum)
+    unsigned* status;
+    int has_mask;
+    int n_tok, n_head, M, n_kv;
+    int n_tiles;              // KV tiles of 128 keys
+    int tiles_per_split;
+    int splits;
+    int rstride;              // rows per split block of part_o / part_ml (= M)
+    int early_dep;            // 1: the grid is one wave; a dependent launch may start after set-up
+    float kq_log2;
+    uint64_t wait_limit_ns;
+    uint32_t probe_iters;
+};
+
+struct SwMaps {
+    CUtensorMap k, v, mask, q16;
+};
+
+struct SwLaunch {
+    SwArgs args;
+    bool pdl;                 // launched right after the qkv_post grid that writes q16
+    const void* q16;
+    const void* k;
+    const void* v;
+    const void* mask;
+    int64_t k_rs, v_rs, m_rs;
+};
+
+// N of the MMA (query rows padded to 16, 32 or 64).
+int rows_n(int M);
+fr_status launch_sw(const SwLaunch& L, int hd, cudaStream_t stream);
+
+}  // namespace sw
 
 // Smallest workspace fr_decode_attn accepts for this shape (0 if unsupported);
 // fr_decode_attn_workspace_size may ask for more so that faster plans fit.

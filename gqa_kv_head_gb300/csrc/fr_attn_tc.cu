@@ -733,7 +733,10 @@ attn_tc_kernel(const __grid_constant__ TcArgs a, const __grid_constant__ Maps mp
     }
 }
 
-// Merge of the split states written in merge-kernel mode. A unit is one (row,
+// Merge of the split states written in merge-kernel mode: split s of row tile
+// rt holds rows [rt*rstride, (rt+1)*rstride) at part_o[((rt*splits + s)*rstride
+// + rr)*HD] (rstride = 128 for the 128-row tiles, M for the keys-on-M kernel).
+// A unit is one (row,
 // 128-column chunk); it gets nw warps (one per split when that fits the GPU in
 // one wave, else one per 6 splits, see launch_merge) and a CTA of up to
 // kMergeWarps warps holds several units. Warp w of a unit takes splits
@@ -748,7 +751,7 @@ constexpr int kMergeSplitsPerWarp = 6;          // nw = ceil(splits / 6) warps p
 template <int HD>
 __global__ void __launch_bounds__(kMergeWarps * 32)
 attn_merge_kernel(const float* __restrict__ part_o, const float2* __restrict__ part_ml, float* __restrict__ out,
-                  int M, int splits, int nw, int early) {
+                  int M, int splits, int nw, int early, int rstride) {
     constexpr int CWM = HD < 128 ? HD : 128;
     constexpr int NCH = HD / CWM;
     constexpr int LANES = CWM / 4;
@@ -764,19 +767,19 @@ attn_merge_kernel(const float* __restrict__ part_o, const float2* __restrict__ p
     const int unit = blockIdx.x * upc + uw;
     const bool live = uw < upc && unit < M * NCH;
     const int row = live ? unit / NCH : 0, chunk = live ? unit - (unit / NCH) * NCH : 0;
-    const int rt = row >> 7, rr = row & 127;
+    const int rt = row / rstride, rr = row - rt * rstride;
     asm volatile("griddepcontrol.wait;" ::: "memory");     // the attention grid is complete
     // A dependent launch (the next call's qkv_post) may start now only when this
     // grid fits in one wave; otherwise its waiting CTAs would hold the SMs the
     // later merge CTAs need.
     if (early) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int n_w = live && splits > warp ? (splits - warp + nw - 1) / nw : 0;   // this warp's splits
-    const float2* ml = part_ml + (int64_t)rt * splits * kRows + rr;
+    const float2* ml = part_ml + (int64_t)rt * splits * rstride + rr;
     const float2 my_ml =
-        lane < n_w ? __ldcg(ml + (int64_t)(warp + nw * lane) * kRows) : make_float2(-INFINITY, 0.f);
+        lane < n_w ? __ldcg(ml + (int64_t)(warp + nw * lane) * rstride) : make_float2(-INFINITY, 0.f);
     float4 v[PER_WARP];
-    const float* base = part_o + ((int64_t)rt * splits * kRows + rr) * HD + chunk * CWM + (lane % LANES) * 4;
-    const int64_t sstride = (int64_t)kRows * HD;
+    const float* base = part_o + ((int64_t)rt * splits * rstride + rr) * HD + chunk * CWM + (lane % LANES) * 4;
+    const int64_t sstride = (int64_t)rstride * HD;
 #pragma unroll
     for (int u = 0; u < PER_WARP; ++u)
         v[u] = (u < n_w && lane < LANES)
@@ -832,25 +835,25 @@ constexpr int kSmallMergeSplits = 8;
 template <int HD>
 __global__ void __launch_bounds__(256)
 attn_merge_small_kernel(const float* __restrict__ part_o, const float2* __restrict__ part_ml,
-                        float* __restrict__ out, int M, int splits) {
+                        float* __restrict__ out, int M, int splits, int rstride) {
     constexpr int CWM = HD < 128 ? HD : 128;
     constexpr int NCH = HD / CWM;
     constexpr int LANES = CWM / 4;
     asm volatile("griddepcontrol.wait;" ::: "memory");     // the attention grid is complete
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int lane = threadIdx.x & 31;
-    const int64_t sstride = (int64_t)kRows * HD;
+    const int64_t sstride = (int64_t)rstride * HD;
     for (int64_t unit = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; unit < (int64_t)M * NCH;
          unit += ((int64_t)gridDim.x * blockDim.x) >> 5) {
         const int row = (int)(unit / NCH), chunk = (int)(unit - (int64_t)row * NCH);
-        const int rt = row >> 7, rr = row & 127;
-        const float2* ml = part_ml + (int64_t)rt * splits * kRows + rr;
-        const float* base = part_o + ((int64_t)rt * splits * kRows + rr) * HD + chunk * CWM + (lane % LANES) * 4;
+        const int rt = row / rstride, rr = row - rt * rstride;
+        const float2* ml = part_ml + (int64_t)rt * splits * rstride + rr;
+        const float* base = part_o + ((int64_t)rt * splits * rstride + rr) * HD + chunk * CWM + (lane % LANES) * 4;
         float2 st[kSmallMergeSplits];
         float4 v[kSmallMergeSplits];
 #pragma unroll
         for (int s2 = 0; s2 < kSmallMergeSplits; ++s2) {
-            st[s2] = s2 < splits ? __ldcg(ml + (int64_t)s2 * kRows) : make_float2(-INFINITY, 0.f);
+            st[s2] = s2 < splits ? __ldcg(ml + (int64_t)s2 * rstride) : make_float2(-INFINITY, 0.f);
             v[s2] = (s2 < splits && lane < LANES) ? __ldcg(reinterpret_cast<const float4*>(base + s2 * sstride))
                                                  : make_float4(0.f, 0.f, 0.f, 0.f);
         }
@@ -881,7 +884,7 @@ attn_merge_small_kernel(const float* __restrict__ part_o, const float2* __restri
 }
 
 fr_status launch_merge(const float* part_o, const float2* part_ml, float* out, int M, int splits, int hd,
-                       cudaStream_t stream) {
+                       int rstride, cudaStream_t stream) {
     if (splits < 1 || splits > kMaxMergeSplits) return FR_ERR_UNSUPPORTED;
     cudaLaunchConfig_t cfg;
     memset(&cfg, 0, sizeof(cfg));
@@ -902,9 +905,9 @@ fr_status launch_merge(const float* part_o, const float2* part_ml, float* out, i
         cfg.numAttrs = 1;
         cudaError_t e;
         switch (hd) {
-            case 64: e = cudaLaunchKernelEx(&cfg, attn_merge_small_kernel<64>, part_o, part_ml, out, M, splits); break;
-            case 128: e = cudaLaunchKernelEx(&cfg, attn_merge_small_kernel<128>, part_o, part_ml, out, M, splits); break;
-            default: e = cudaLaunchKernelEx(&cfg, attn_merge_small_kernel<256>, part_o, part_ml, out, M, splits); break;
+            case 64: e = cudaLaunchKernelEx(&cfg, attn_merge_small_kernel<64>, part_o, part_ml, out, M, splits, rstride); break;
+            case 128: e = cudaLaunchKernelEx(&cfg, attn_merge_small_kernel<128>, part_o, part_ml, out, M, splits, rstride); break;
+            default: e = cudaLaunchKernelEx(&cfg, attn_merge_small_kernel<256>, part_o, part_ml, out, M, splits, rstride); break;
         }
         return e == cudaSuccess ? FR_OK : FR_ERR_CUDA;
     }
@@ -938,9 +941,9 @@ fr_status launch_merge(const float* part_o, const float2* part_ml, float* out, i
     cfg.numAttrs = 1;
     cudaError_t e;
     switch (hd) {
-        case 64: e = cudaLaunchKernelEx(&cfg, attn_merge_kernel<64>, part_o, part_ml, out, M, splits, nw, early); break;
-        case 128: e = cudaLaunchKernelEx(&cfg, attn_merge_kernel<128>, part_o, part_ml, out, M, splits, nw, early); break;
-        default: e = cudaLaunchKernelEx(&cfg, attn_merge_kernel<256>, part_o, part_ml, out, M, splits, nw, early); break;
+        case 64: e = cudaLaunchKernelEx(&cfg, attn_merge_kernel<64>, part_o, part_ml, out, M, splits, nw, early, rstride); break;
+        case 128: e = cudaLaunchKernelEx(&cfg, attn_merge_kernel<128>, part_o, part_ml, out, M, splits, nw, early, rstride); break;
+        default: e = cudaLaunchKernelEx(&cfg, attn_merge_kernel<256>, part_o, part_ml, out, M, splits, nw, early, rstride); break;
     }
     return e == cudaSuccess ? FR_OK : FR_ERR_CUDA;
 }
@@ -971,6 +974,19 @@ static bool encode_2d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t
     return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool encode_f16_2d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows, uint64_t row_stride,
+                   uint32_t box_inner, uint32_t box_rows, bool swizzle128) {
+    auto enc = get_encoder();
+    if (!enc) return false;
+    cuuint64_t dims[2] = {inner, rows};
+    cuuint64_t strides[1] = {row_stride * 2};
+    cuuint32_t box[2] = {box_inner, box_rows};
+    cuuint32_t es[2] = {1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 // 2-D fp32 tensor [rows][inner], contiguous rows; boxes of 32 columns (128 B) x

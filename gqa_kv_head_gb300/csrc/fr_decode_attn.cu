@@ -409,10 +409,27 @@ static size_t tc_merge_workspace_bytes(int M, int hd) {
     return tc_merge_fixed_bytes(M, hd) + (size_t)tc_merge_max_splits(M) * tc_merge_split_bytes(M, hd);
 }
 
-// Smallest workspace any plan of this shape accepts (in-kernel merge); the
-// mma.sync engine's needs count only for the shapes it takes.
-static size_t workspace_bytes_for(int n_tok, int n_head, int hd, int n_kv) {
+// The kernel with the KV tile on the MMA's M side: M <= 64 decode rows, hd 128
+// or 256, library-chosen clusters and merge. One KV split of 128-key tiles per
+// SM; the split count is cut to what the workspace holds (a single split
+// needs no partial states).
+static bool sw_shape_ok(int n_tok, int n_head, int hd) {
+    return (hd == 128 || hd == 256) && n_tok <= kMaskWin && (int64_t)n_tok * n_head <= sw::kMaxRows;
+}
+static bool use_sw(int n_tok, int n_head, int hd, const fr_attn_opts& o) {
+    if (o.engine != 0 || !sw_shape_ok(n_tok, n_head, hd)) return false;
+    if (o.layout == 2) return true;
+    if (o.layout == 1 || o.force_cluster != 0 || o.merge_mode == 1) return false;
+    return true;
+}
+
+// Smallest workspace the plan a call with these options takes accepts: the
+// keys-on-M kernel needs only the header and the f16 Q slot (it cuts its split
+// count to what the workspace holds); the 128-row kernel its in-launch merge
+// plan; the mma.sync engine's needs count for the shapes it takes.
+static size_t workspace_bytes_for(int n_tok, int n_head, int hd, int n_kv, const fr_attn_opts& o) {
     const int M = n_tok * n_head;
+    if (use_sw(n_tok, n_head, hd, o)) return kWsHeader + tc_q16_bytes(M, hd);
     const size_t b = tc_workspace_bytes(M, hd);
     if (!decode_shape(n_tok, n_head)) return b;
     const size_t a = v1_workspace_bytes(M, hd, n_kv);
@@ -503,6 +520,27 @@ static TcPlan choose_tc_plan(int M, int hd, int n_kv, int num_sms, const fr_attn
     return p;
 }
 
+static size_t sw_split_bytes(int M, int hd) { return (size_t)M * (hd * sizeof(float) + sizeof(float2)); }
+
+struct SwPlan {
+    int n_tiles, splits, tiles_per_split;
+};
+
+static SwPlan make_sw_plan(int M, int hd, int n_kv, int num_sms, int force_splits, size_t ws_bytes) {
+    SwPlan p;
+    p.n_tiles = (n_kv + 127) / 128;
+    int S = force_splits > 0 ? force_splits : num_sms;
+    S = max(1, min(S, min(p.n_tiles, min(num_sms, tc::kMaxMergeSplits))));
+    if (S > 1) {
+        const size_t fixed = kWsHeader + tc_q16_bytes(M, hd);
+        const size_t fit = ws_bytes > fixed ? (ws_bytes - fixed) / sw_split_bytes(M, hd) : 0;
+        if ((size_t)S > fit) S = fit > 1 ? (int)fit : 1;
+    }
+    p.tiles_per_split = (p.n_tiles + S - 1) / S;
+    p.splits = (p.n_tiles + p.tiles_per_split - 1) / p.tiles_per_split;
+    return p;
+}
+
 template <int HD>
 static cudaError_t ensure_smem_attr(int dev) {
     static unsigned long long done = 0ull;     // one bit per device (idempotent)
@@ -533,7 +571,8 @@ static fr_status decode_attn_impl(const uint16_t* q16, const float* q, int64_t q
     memset(&o, 0, sizeof(o));
     if (opts) o = *opts;
     if (o.engine < 0 || o.engine > 1 || o.force_splits < 0 || o.wait_probe_iters < 0) return FR_ERR_INVALID_ARG;
-    if (o.merge_mode < 0 || o.merge_mode > 2) return FR_ERR_INVALID_ARG;
+    if (o.merge_mode < 0 || o.merge_mode > 2 || o.layout < 0 || o.layout > 2) return FR_ERR_INVALID_ARG;
+    if (o.layout == 2 && (o.engine != 0 || !sw_shape_ok(n_tok, n_head, hd))) return FR_ERR_UNSUPPORTED;
     if (o.force_cluster != 0 && o.force_cluster != 1 && o.force_cluster != 2 && o.force_cluster != 4 &&
         o.force_cluster != 8)
         return FR_ERR_INVALID_ARG;
@@ -558,7 +597,7 @@ static fr_status decode_attn_impl(const uint16_t* q16, const float* q, int64_t q
         if (!build_rope_table(rp, resolve_q_scale(q_scale, hd), hd, &tb)) return FR_ERR_INVALID_ARG;
     }
     const int M = n_tok * n_head;
-    if (ws_bytes < workspace_bytes_for(n_tok, n_head, hd, n_kv)) return FR_ERR_WORKSPACE;
+    if (ws_bytes < workspace_bytes_for(n_tok, n_head, hd, n_kv, o)) return FR_ERR_WORKSPACE;
 
     int dev = 0, sms = 152;
     if (cudaGetDevice(&dev) != cudaSuccess) return FR_ERR_CUDA;
@@ -569,6 +608,50 @@ static fr_status decode_attn_impl(const uint16_t* q16, const float* q, int64_t q
         return FR_ERR_INVALID_ARG;
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return FR_ERR_CUDA;
     unsigned char* w = static_cast<unsigned char*>(ws);
+
+    if (use_sw(n_tok, n_head, hd, o)) {
+        const SwPlan p = make_sw_plan(M, hd, n_kv, sms, o.force_splits, ws_bytes);
+        sw::SwLaunch L;
+        memset(&L, 0, sizeof(L));
+        sw::SwArgs& a = L.args;
+        unsigned char* qslot = w + kWsHeader;
+        unsigned char* parts = qslot + tc_q16_bytes(M, hd);
+        if (q16) {
+            L.q16 = q16;
+        } else {
+            const fr_status st = launch_qkv_post(q, q_tok_stride, pos, n_tok, n_head, hd, tb,
+                                                 reinterpret_cast<uint16_t*>(qslot), nullptr, stream);
+            if (st != FR_OK) return st;
+            L.q16 = qslot;
+            L.pdl = true;
+        }
+        a.out = out;
+        a.status = reinterpret_cast<unsigned*>(w);
+        a.part_o = reinterpret_cast<float*>(parts);
+        a.part_ml = reinterpret_cast<float2*>(parts + (size_t)p.splits * M * hd * sizeof(float));
+        a.has_mask = mask != nullptr;
+        a.n_tok = n_tok;
+        a.n_head = n_head;
+        a.M = M;
+        a.n_kv = n_kv;
+        a.n_tiles = p.n_tiles;
+        a.tiles_per_split = p.tiles_per_split;
+        a.splits = p.splits;
+        a.rstride = M;
+        a.early_dep = 1;                     // at most one CTA per SM: one wave
+        a.kq_log2 = kq_scale * kLog2e;
+        a.wait_limit_ns = tc::kWaitLimitNs;
+        a.probe_iters = (uint32_t)o.wait_probe_iters;
+        L.k = k;
+        L.v = v;
+        L.mask = mask;
+        L.k_rs = k_rs;
+        L.v_rs = v_rs;
+        L.m_rs = m_rs;
+        const fr_status st = sw::launch_sw(L, hd, stream);
+        if (st != FR_OK || p.splits == 1) return st;
+        return tc::launch_merge(a.part_o, a.part_ml, out, M, p.splits, hd, M, stream);
+    }
 
     if (o.engine == 0) {
         bool plan_ok = true;
@@ -624,7 +707,7 @@ static fr_status decode_attn_impl(const uint16_t* q16, const float* q, int64_t q
         L.bn = p.bn;
         const fr_status st = tc::launch_tc(L, hd, stream);
         if (st != FR_OK || !p.merge_kernel) return st;
-        return tc::launch_merge(a.part_o, a.part_ml, out, M, p.splits, hd, stream);
+        return tc::launch_merge(a.part_o, a.part_ml, out, M, p.splits, hd, 128, stream);
     }
 
     const Plan p = make_plan(M, n_kv, sms, o.force_splits);
@@ -667,10 +750,17 @@ extern "C" size_t fr_decode_attn_workspace_size(int n_tok, int n_head, int hd, i
     if (!tc_shape_ok(n_tok, n_head)) return 0;
     if ((hd != 64 && hd != 128 && hd != 256) || n_kv < 1 || n_kv > (1 << 26)) return 0;
     const int M = n_tok * n_head;
-    // room for every plan, the merge-kernel one included
-    const size_t base = workspace_bytes_for(n_tok, n_head, hd, n_kv);
+    // room for every plan, forced ones and the merge-kernel one included
+    fr_attn_opts o;
+    memset(&o, 0, sizeof(o));
+    o.layout = 1;                        // the 128-row kernel's in-launch plan (and engine 1's)
+    const size_t base = workspace_bytes_for(n_tok, n_head, hd, n_kv, o);
     const size_t merge = tc_merge_max_splits(M) >= 1 ? tc_merge_workspace_bytes(M, hd) : 0;
-    return merge > base ? merge : base;
+    const size_t sw_full = sw_shape_ok(n_tok, n_head, hd)
+                               ? kWsHeader + tc_q16_bytes(M, hd) + (size_t)tc::kMaxMergeSplits * sw_split_bytes(M, hd)
+                               : 0;
+    size_t r = merge > base ? merge : base;
+    return sw_full > r ? sw_full : r;
 }
 
 extern "C" fr_status fr_decode_attn_plan(int n_tok, int n_head, int hd, int n_kv, int fused_qkv_post,
@@ -680,20 +770,29 @@ extern "C" fr_status fr_decode_attn_plan(int n_tok, int n_head, int hd, int n_kv
     fr_attn_opts o;
     memset(&o, 0, sizeof(o));
     if (opts) o = *opts;
-    if (o.engine < 0 || o.engine > 1 || o.force_splits < 0 || o.merge_mode < 0 || o.merge_mode > 2)
+    if (o.engine < 0 || o.engine > 1 || o.force_splits < 0 || o.merge_mode < 0 || o.merge_mode > 2 ||
+        o.layout < 0 || o.layout > 2)
         return FR_ERR_INVALID_ARG;
+    if (o.layout == 2 && (o.engine != 0 || !sw_shape_ok(n_tok, n_head, hd))) return FR_ERR_UNSUPPORTED;
     if (o.force_cluster != 0 && o.force_cluster != 1 && o.force_cluster != 2 && o.force_cluster != 4 &&
         o.force_cluster != 8)
         return FR_ERR_INVALID_ARG;
     const int M = n_tok * n_head;
     if (o.engine == 1 && !decode_shape(n_tok, n_head)) return FR_ERR_UNSUPPORTED;
-    if (workspace_bytes < workspace_bytes_for(n_tok, n_head, hd, n_kv)) return FR_ERR_WORKSPACE;
+    if (workspace_bytes < workspace_bytes_for(n_tok, n_head, hd, n_kv, o)) return FR_ERR_WORKSPACE;
     int dev = 0, sms = 152;
     if (cudaGetDevice(&dev) != cudaSuccess) return FR_ERR_CUDA;
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return FR_ERR_CUDA;
     memset(plan, 0, sizeof(*plan));
     plan->engine = o.engine;
-    if (o.engine == 0) {
+    if (use_sw(n_tok, n_head, hd, o)) {
+        const SwPlan p = make_sw_plan(M, hd, n_kv, sms, o.force_splits, workspace_bytes);
+        plan->row_tiles = 1;
+        plan->splits = p.splits;
+        plan->cluster = 1;
+        plan->merge_kernel = p.splits > 1 ? 1 : 0;
+        plan->keys_on_m = 1;
+    } else if (o.engine == 0) {
         bool ok = true;
         const TcPlan p = choose_tc_plan(M, hd, n_kv, sms, o, workspace_bytes, &ok);
         if (!ok) return FR_ERR_WORKSPACE;
@@ -715,7 +814,9 @@ extern "C" fr_status fr_decode_attn_plan(int n_tok, int n_head, int hd, int n_kv
 namespace fr {
 size_t decode_attn_min_workspace_bytes(int n_tok, int n_head, int hd, int n_kv) {
     if (fr_decode_attn_workspace_size(n_tok, n_head, hd, n_kv) == 0) return 0;
-    return workspace_bytes_for(n_tok, n_head, hd, n_kv);
+    fr_attn_opts o;
+    memset(&o, 0, sizeof(o));
+    return workspace_bytes_for(n_tok, n_head, hd, n_kv, o);
 }
 }  // namespace fr
 

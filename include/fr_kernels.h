@@ -248,6 +248,11 @@ typedef struct fr_attn_opts {
                               attention launch (clusters + arrival tickets); 2 = a separate
                               merge kernel (split count cut to what the workspace holds;
                               FR_ERR_WORKSPACE if forced splits do not fit) */
+    int layout;            /* 0 = library's choice; 1 = 128-row query tiles (the query rows
+                              are the MMA's M); 2 = 128-key tiles as the MMA's M and the
+                              query rows as its N (M <= 64 rows, hd 128 or 256, n_tok <= 16:
+                              FR_ERR_UNSUPPORTED otherwise). The library's choice is 2 where
+                              it applies, unless force_cluster or merge_mode 1 is given. */
 } fr_attn_opts;
 
 fr_status fr_decode_attn_ex(const uint16_t* q16,
@@ -274,6 +279,7 @@ typedef struct fr_attn_plan {
     int cluster;           /* CTAs per thread-block cluster (1 = none) */
     int merge_kernel;      /* 1: split states merged by a separate kernel */
     int launches;          /* kernels one call launches (qkv_post, attention, merge) */
+    int keys_on_m;         /* 1: 128-key tiles are the MMA's M, the query rows its N */
 } fr_attn_plan;
 
 fr_status fr_decode_attn_plan(int n_tok, int n_head, int hd, int n_kv, int fused_qkv_post,
