@@ -71,10 +71,13 @@ struct SwArgs {
     float* part_o;            // [splits][rstride][hd] unnormalised O rows (splits > 1)
     float2* part_ml;          // [splits][rstride] (row max in log2 units, row sum)
     unsigned* status;
+    const float* q;           // f32 Q rows when the kernel ropes them itself (rope_in_kernel)
+    int64_t q_tok_stride;
+    const int32_t* pos;
+    int rope_in_kernel;       // 1: build the f16 Q tile from q/pos (qkv_post's arithmetic); 0: load q16
     int has_mask;
     int n_tok, n_head, M, n_kv;
-    int n_tiles;              // KV tiles of 128 keys
-    int tiles_per_split;
+    int keys_per_split;       // a multiple of 16; split s reads keys [s*kps, min(n_kv, (s+1)*kps))
     int splits;
     int rstride;              // rows per split block of part_o / part_ml (= M)
     int early_dep;            // 1: the grid is one wave; a dependent launch may start after set-up
@@ -89,7 +92,8 @@ struct SwMaps {
 
 struct SwLaunch {
     SwArgs args;
-    bool pdl;                 // launched right after the qkv_post grid that writes q16
+    RopeTable tb;             // rope_in_kernel only
+    bool pdl;                 // programmatic dependent launch (the kernel waits before reading inputs)
     const void* q16;
     const void* k;
     const void* v;

@@ -10,24 +10,30 @@
 // padding; here 128 keys are the MMA's M and the query rows its N (16, 32 or
 // 64), so the tensor work follows the real rows.
 //
-// One CTA = one KV split (one CTA per SM), 192 threads:
-//   warps 0-3  softmax, one thread per key of the tile (TMEM lane = key of
-//              S^T): kq_scale and the mask, row maxima over the 128 keys (warp
-//              shuffles, then the four warps through shared memory), lazy
-//              rescaling (only when a row maximum grows by more than 2^8),
-//              P = 2^(s - m) as two f16 terms P_hi + P_lo written to shared
-//              memory as the B operand [P_hi; P_lo] of the PV MMA, and partial
-//              row sums per thread. After the loop the same threads own the
-//              TMEM lanes of O^T (lane = head dim) for the epilogue, where
-//              O = O_hi + O_lo.
-//   warp 4     TMA producer: one ring of 32 KiB stages (128 keys x 128 dims of
+// One CTA = one KV split (one CTA per SM), 320 threads:
+//   warps 0-7  softmax, one thread per (key of the tile, half of the query
+//              rows): warps w and w + 4 share TMEM lane quadrant w (keys
+//              32w..32w+31 of S^T) and take rows [0, NQ/2) and [NQ/2, NQ).
+//              kq_scale and the mask; the per-row reference maxima are only
+//              recomputed when some score exceeds its row's reference by more
+//              than 2^8 (one barrier-OR vote per tile; the row maxima then come
+//              from warp shuffles and the four lane quadrants through shared
+//              memory, and O and the partial sums are rescaled); P = 2^(s - m)
+//              as two f16 terms P_hi + P_lo, written MN-major (one 128-byte row
+//              per key) as the B operand of the PV MMA; partial row sums per
+//              thread. After the loop the same threads own the TMEM lanes of
+//              O^T (lane = head dim) for the epilogue, where O = O_hi + O_lo.
+//   warp 8     TMA producer: one ring of 32 KiB stages (128 keys x 128 dims of
 //              K or of V, two 64-dim boxes) filled in exactly the order the
-//              MMAs consume them, and a ring of mask tiles.
-//   warp 5     MMA issuer: S^T_j = K_j Q^T (A = K stage, K-major; B = the Q
-//              rows), O^T += V_j^T [P_hi; P_lo]^T (A = V stage read MN-major,
-//              N = 2 x rows: the P_lo product accumulates in its own columns).
+//              MMAs consume them, a ring of mask tiles, and in the fused call
+//              the f32 Q rows (one bulk copy per token) for the in-kernel RoPE.
+//   warp 9     MMA issuer: S^T_j = K_j Q^T (A = K stage, K-major; B = the Q
+//              rows), O^T += V_j^T [P_hi; P_lo]^T (A = V stage and B = P^T, both
+//              read MN-major; the P_lo product accumulates in its own columns).
 //              S_{j+1} is issued before PV_j, so the softmax of tile j+1
 //              overlaps PV_j.
+// In the fused call the kernel ropes the Q rows itself with qkv_post's
+// arithmetic (fr_qkv_post's device routines), so one call is one launch.
 // Each split writes its unnormalised O rows with its row maxima (log2 units)
 // and sums to the workspace, and attn_merge_kernel combines them; a single
 // split normalises and writes the output rows itself.
@@ -48,14 +54,15 @@ namespace sw {
 using namespace sm100;
 
 constexpr int kKeys = 128;               // keys per KV tile = the MMA's M
-constexpr int kSmaxThreads = 128;        // warps 0-3
-constexpr int kProdWarp = 4;
-constexpr int kMmaWarp = 5;
-constexpr int kThreads = 192;
+constexpr int kSmaxWarps = 8;            // two per TMEM lane quadrant
+constexpr int kSmaxThreads = kSmaxWarps * 32;
+constexpr int kProdWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr int kThreads = (kSmaxWarps + 2) * 32;
 constexpr float kTau = 8.0f;
 constexpr float kLog2e = 1.4426950408889634f;
-constexpr int kBox = 16384;              // 128 keys x 64 dims f16 (128-byte rows, 128-byte swizzle)
-constexpr int kStage = 2 * kBox;         // 128 keys x 128 dims
+constexpr int kBox = 16384;              // 128 rows x 128 bytes (64 f16), 128-byte swizzle
+constexpr int kStage = 2 * kBox;         // 128 keys x 128 dims of K or V
 constexpr int kSmemLimit = 232448;
 
 template <int HD, int NQ>
@@ -63,11 +70,11 @@ struct Cfg {
     static_assert(HD == 128 || HD == 256, "head dims");
     static_assert(NQ == 16 || NQ == 32 || NQ == 64, "query rows");
     static constexpr int HALVES = HD / 128;          // K (and V) stages per tile
-    static constexpr int Q_BOX = NQ * 128;           // 64 dims of the NQ rows
+    static constexpr int RH = NQ / 2;                // rows per softmax thread
+    static constexpr int N2 = 2 * NQ < 64 ? 64 : 2 * NQ;   // PV MMA N: [P_hi | P_lo | zeros]
+    static constexpr int Q_BOX = NQ * 128;           // 64 dims of the NQ rows (K-major)
     static constexpr int Q_BYTES = (HD / 64) * Q_BOX;
-    static constexpr int P_ROWS = 2 * NQ;            // [P_hi; P_lo]
-    static constexpr int P_BOX = P_ROWS * 128;       // 64 keys of every P row
-    static constexpr int P_BYTES = 2 * P_BOX;        // 128 keys
+    static constexpr int P_BYTES = (N2 / 64) * kBox; // P^T: 128 keys x N2 (MN-major, 64 columns per box)
     static constexpr int MASK_BOX = kMaskWin * 128;  // <= 16 token rows x 64 keys, unswizzled
     static constexpr int MASK_BYTES = 2 * MASK_BOX;
     static constexpr int MS = 3;                     // mask slots
@@ -83,33 +90,36 @@ struct Cfg {
     static constexpr int BAR_OFF = AUX_OFF + AUX;
     static constexpr int SMEM = BAR_OFF + 1024 + 1024;   // barriers + TMEM word, + alignment slack
     static_assert(SMEM <= kSmemLimit, "shared memory budget");
-    static_assert(Q_BOX % 1024 == 0 || NQ == 16, "Q boxes");
-    static_assert(P_BOX % 1024 == 0 && MASK_BOX % 1024 == 0, "1024-B alignment of swizzled tiles");
-    // aux: [4][NQ] per-warp partial maxima / sums, [NQ] row max m, [NQ] rescale
-    // factors, [NQ] row sums l, two rescale flags
+    static_assert(Q_BYTES % 1024 == 0 && MASK_BOX % 1024 == 0, "1024-B alignment of swizzled tiles");
+    // the f32 Q rows of the fused call land in the P buffers (free until the
+    // first P tile, which comes after QFULL)
+    static_assert(NQ * HD * 4 <= 2 * P_BYTES, "f32 Q rows in the P buffers");
+    // aux: [4][NQ] per-quadrant partial maxima / sums, [NQ] row max m, [NQ]
+    // rescale factors, [NQ] row sums l, a flag; then the RoPE table
     static constexpr int AUX_RED = 0;
     static constexpr int AUX_M = 4 * NQ * 4;
     static constexpr int AUX_A = AUX_M + NQ * 4;
     static constexpr int AUX_L = AUX_A + NQ * 4;
     static constexpr int AUX_FLAG = AUX_L + NQ * 4;
-    static_assert(AUX_FLAG + 16 <= AUX, "aux");
+    static constexpr int AUX_TB = (AUX_FLAG + 16 + 15) / 16 * 16;
+    static_assert(AUX_TB + (int)sizeof(RopeTable) <= AUX, "aux");
     static constexpr int B_FULL = 0, B_EMPTY = R, B_MFULL = 2 * R, B_MEMPTY = 2 * R + MS,
                          B_SFULL = 2 * (R + MS), B_PFULL = B_SFULL + 2, B_ODONE = B_SFULL + 4,
                          B_QFULL = B_SFULL + 5, B_MMADONE = B_SFULL + 6, B_PROBE = B_SFULL + 7,
-                         N_BARS = B_SFULL + 8;
+                         B_QF32 = B_SFULL + 8, N_BARS = B_SFULL + 9;
     static constexpr int TMEM_SLOT = 120 * 8;
     static_assert(N_BARS <= 120, "barrier slots");
     // TMEM columns: S^T double buffer (NQ each), then O^T per 128-dim half
-    // (2NQ: O_hi^T, O_lo^T)
+    // (N2: O_hi^T in [0, NQ), O_lo^T in [NQ, 2NQ))
     static constexpr int TM_S = 0;
     static constexpr int TM_O = 2 * NQ;
-    static constexpr int TM_USED = TM_O + HALVES * 2 * NQ;
+    static constexpr int TM_USED = TM_O + HALVES * N2;
     static constexpr uint32_t TM_COLS = TM_USED <= 32 ? 32u : TM_USED <= 64 ? 64u : TM_USED <= 128 ? 128u
                                         : TM_USED <= 256 ? 256u : 512u;
 };
 
 // Reduce-scatter across the 32 lanes of a warp (maximum or sum) of CH values
-// per lane (CH = 16 or 32): at each step the lanes with bit S set keep the
+// per lane (CH = 8, 16 or 32): at each step the lanes with bit S set keep the
 // upper half of the values and their partners the lower half, so that after
 // log2(CH) steps a lane holds one value, reduced over the lanes that differ
 // in the bits used so far; the remaining steps reduce over the other bits.
@@ -152,26 +162,47 @@ __device__ __forceinline__ int rs_row(int lane) {
 
 __device__ __forceinline__ void record_timeout(unsigned* status, unsigned bit) { atomicOr(status, bit); }
 
-// Barrier over the four softmax warps (named barrier 1).
+// Barrier over the softmax warps (named barrier 1).
 __device__ __forceinline__ void softmax_bar_sync() {
     asm volatile("bar.sync 1, %0;" :: "n"(kSmaxThreads) : "memory");
+}
+// The same barrier, returning whether any softmax thread passed a true vote.
+__device__ __forceinline__ bool softmax_bar_any(bool vote) {
+    uint32_t r;
+    asm volatile("{ .reg .pred p, q; setp.ne.u32 q, %1, 0; bar.red.or.pred p, 1, %2, q; selp.u32 %0, 1, 0, p; }"
+                 : "=r"(r) : "r"((uint32_t)vote), "n"(kSmaxThreads) : "memory");
+    return r != 0;
 }
 
 template <int N>
 __device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, float* x) {
-    if constexpr (N == 16) {
+    if constexpr (N == 8) {
+        tmem_ld_x8(taddr, reinterpret_cast<uint32_t*>(x));
+    } else if constexpr (N == 16) {
         tmem_ld_x16(taddr, reinterpret_cast<uint32_t*>(x));
     } else {
 #pragma unroll
         for (int c = 0; c < N; c += 32) tmem_ld_x32(taddr + c, reinterpret_cast<uint32_t*>(x) + c);
     }
 }
+template <int N>
+__device__ __forceinline__ void tmem_st_cols(uint32_t taddr, const float* x) {
+    if constexpr (N == 8) {
+        tmem_st_x8(taddr, reinterpret_cast<const uint32_t*>(x));
+    } else if constexpr (N == 16) {
+        tmem_st_x16(taddr, reinterpret_cast<const uint32_t*>(x));
+    } else {
+#pragma unroll
+        for (int c = 0; c < N; c += 32) tmem_st_x32(taddr + c, reinterpret_cast<const uint32_t*>(x) + c);
+    }
+}
 
 template <int HD, int NQ>
 __global__ void __launch_bounds__(kThreads, 1)
-attn_sw_kernel(const __grid_constant__ SwArgs a, const __grid_constant__ SwMaps mp) {
+attn_sw_kernel(const __grid_constant__ SwArgs a, const __grid_constant__ SwMaps mp,
+               const __grid_constant__ RopeTable tb) {
     using C = Cfg<HD, NQ>;
-    constexpr int CH = NQ < 32 ? NQ : 32;                // rows per reduction chunk
+    constexpr int RH = C::RH;
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     unsigned char* sm = reinterpret_cast<unsigned char*>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     uint64_t* bars = reinterpret_cast<uint64_t*>(sm + C::BAR_OFF);
@@ -180,12 +211,13 @@ attn_sw_kernel(const __grid_constant__ SwArgs a, const __grid_constant__ SwMaps 
     float* sM = reinterpret_cast<float*>(sm + C::AUX_OFF + C::AUX_M);         // [NQ] row max (log2 units)
     float* sA = reinterpret_cast<float*>(sm + C::AUX_OFF + C::AUX_A);         // [NQ] rescale factors
     float* sL = reinterpret_cast<float*>(sm + C::AUX_OFF + C::AUX_L);         // [NQ] row sums
-    int* sFlag = reinterpret_cast<int*>(sm + C::AUX_OFF + C::AUX_FLAG);       // [2] some row rescaled
+    int* sFlag = reinterpret_cast<int*>(sm + C::AUX_OFF + C::AUX_FLAG);       // some row's reference grew
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int split = blockIdx.x;
-    const int t0 = split * a.tiles_per_split;
-    const int n_my = max(0, min(a.n_tiles, t0 + a.tiles_per_split) - t0);
+    const int k_begin = split * a.keys_per_split;                   // this split's keys
+    const int k_end = min(a.n_kv, k_begin + a.keys_per_split);
+    const int n_my = k_end > k_begin ? (k_end - k_begin + kKeys - 1) / kKeys : 0;   // tiles (the last may be short)
     const uint64_t limit = a.wait_limit_ns;
     bool failed = false;                 // after a first timeout, later waits give up at once
     auto wait = [&](uint32_t b, uint32_t parity) {
@@ -204,35 +236,36 @@ attn_sw_kernel(const __grid_constant__ SwArgs a, const __grid_constant__ SwMaps 
         }
         for (int s = 0; s < C::MS; ++s) {
             mbar_init(bar(C::B_MFULL + s), 1);
-            mbar_init(bar(C::B_MEMPTY + s), 4);              // one arrival per softmax warp
+            mbar_init(bar(C::B_MEMPTY + s), kSmaxWarps);     // one arrival per softmax warp
         }
         mbar_init(bar(C::B_SFULL + 0), 1);
         mbar_init(bar(C::B_SFULL + 1), 1);
         mbar_init(bar(C::B_PFULL + 0), kSmaxThreads);
         mbar_init(bar(C::B_PFULL + 1), kSmaxThreads);
         mbar_init(bar(C::B_ODONE), 1);
-        mbar_init(bar(C::B_QFULL), 1);
+        mbar_init(bar(C::B_QFULL), a.rope_in_kernel ? kSmaxThreads : 1);
         mbar_init(bar(C::B_MMADONE), 1);
         mbar_init(bar(C::B_PROBE), 1);
+        mbar_init(bar(C::B_QF32), 1);
         mbar_fence_init();
         prefetch_tmap(&mp.k);
         prefetch_tmap(&mp.v);
-        prefetch_tmap(&mp.q16);
+        if (!a.rope_in_kernel) prefetch_tmap(&mp.q16);
     }
     if (tid < NQ) {
         sM[tid] = -INFINITY;
         sA[tid] = 1.f;
         sL[tid] = 0.f;
     }
-    if (tid < 2) sFlag[tid] = 0;
+    if (tid == 0) sFlag[0] = 0;
     if (warp == kMmaWarp) tmem_alloc(smem_addr(sTmemBase), C::TM_COLS);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tbase = *sTmemBase;
-    // a dependent grid (the merge kernel, or the next call's qkv_post) may be
-    // scheduled now; it waits for this grid's completion before reading what
-    // this grid writes. Only when this grid is one wave.
+    // a dependent grid (the merge kernel, or the next call) may be scheduled
+    // now; it waits for this grid's completion before reading what this grid
+    // writes. Only when this grid is one wave.
     if (a.early_dep) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
     const int n_units = 2 * n_my;                        // K_0, K_1, V_0, K_2, V_1, ..., V_{n-1}
@@ -264,7 +297,7 @@ attn_sw_kernel(const __grid_constant__ SwArgs a, const __grid_constant__ SwMaps 
                 const int st = p % C::R;
                 const uint32_t dst = smem_addr(sm + C::RING_OFF + st * kStage);
                 const CUtensorMap* m = is_v ? &mp.v : &mp.k;
-                const int y = (t0 + tile) * kKeys;
+                const int y = k_begin + tile * kKeys;
                 mbar_expect_tx(bar(C::B_FULL + st), (uint32_t)kStage);
                 tma_load_2d(dst, m, (2 * h) * 64, y, bar(C::B_FULL + st));
                 tma_load_2d(dst + kBox, m, (2 * h + 1) * 64, y, bar(C::B_FULL + st));
@@ -273,18 +306,28 @@ attn_sw_kernel(const __grid_constant__ SwArgs a, const __grid_constant__ SwMaps 
                 const int st = i % C::MS;
                 const uint32_t dst = smem_addr(sm + C::M_OFF + st * C::MASK_BYTES);
                 mbar_expect_tx(bar(C::B_MFULL + st), mask_tx);
-                tma_load_2d(dst, &mp.mask, (t0 + i) * kKeys, 0, bar(C::B_MFULL + st));
-                tma_load_2d(dst + C::MASK_BOX, &mp.mask, (t0 + i) * kKeys + 64, 0, bar(C::B_MFULL + st));
+                tma_load_2d(dst, &mp.mask, k_begin + i * kKeys, 0, bar(C::B_MFULL + st));
+                tma_load_2d(dst + C::MASK_BOX, &mp.mask, k_begin + i * kKeys + 64, 0, bar(C::B_MFULL + st));
             };
-            // K/V and mask tiles need no Q: the first ones go out before the wait
-            // for the grid that writes the Q rows
+            // launched as a programmatic dependent: no input is read before the
+            // grids ahead of this one on the stream are complete (one of them
+            // may have written the KV rows or the Q rows)
+            asm volatile("griddepcontrol.wait;" ::: "memory");
+            if (a.rope_in_kernel) {
+                // the f32 Q rows, one bulk copy per token (its n_head rows are contiguous)
+                const uint32_t row_bytes = (uint32_t)(a.n_head * HD * 4);
+                mbar_expect_tx(bar(C::B_QF32), row_bytes * (uint32_t)a.n_tok);
+                for (int t = 0; t < a.n_tok; ++t)
+                    bulk_load(smem_addr(sm + C::P_OFF + t * row_bytes), a.q + (int64_t)t * a.q_tok_stride, row_bytes,
+                              bar(C::B_QF32));
+            } else {
+                mbar_expect_tx(bar(C::B_QFULL), (uint32_t)C::Q_BYTES);
+                for (int b = 0; b < HD / 64; ++b)
+                    tma_load_2d(smem_addr(sm + C::Q_OFF + b * C::Q_BOX), &mp.q16, b * 64, 0, bar(C::B_QFULL));
+            }
             int np = 0, nm = 0;
             for (; np < min(C::R, n_pieces); ++np) load_piece(np);
             for (; nm < min(C::MS, n_masks); ++nm) load_mask(nm);
-            asm volatile("griddepcontrol.wait;" ::: "memory");
-            mbar_expect_tx(bar(C::B_QFULL), (uint32_t)C::Q_BYTES);
-            for (int b = 0; b < HD / 64; ++b)
-                tma_load_2d(smem_addr(sm + C::Q_OFF + b * C::Q_BOX), &mp.q16, b * 64, 0, bar(C::B_QFULL));
             uint64_t t_last = global_ns();
             while (np < n_pieces || nm < n_masks) {
                 bool moved = false;
@@ -312,7 +355,7 @@ attn_sw_kernel(const __grid_constant__ SwArgs a, const __grid_constant__ SwMaps 
                 if (!mbar_wait(bar(C::B_FULL + i % C::R), (i / C::R) & 1, limit)) record_timeout(a.status, 1u);
             for (int i = max(0, nm - C::MS); i < nm; ++i)
                 if (!mbar_wait(bar(C::B_MFULL + i % C::MS), (i / C::MS) & 1, limit)) record_timeout(a.status, 1u);
-            if (!mbar_wait(bar(C::B_QFULL), 0, limit)) record_timeout(a.status, 1u);
+            if (!mbar_wait(bar(a.rope_in_kernel ? C::B_QF32 : C::B_QFULL), 0, limit)) record_timeout(a.status, 1u);
         }
         if (a.probe_iters && lane == 1) {
             // test hook: a bounded wait on a barrier nothing ever signals
@@ -323,7 +366,7 @@ attn_sw_kernel(const __grid_constant__ SwArgs a, const __grid_constant__ SwMaps 
             if (!mbar_wait(bar(C::B_QFULL), 0, limit)) record_timeout(a.status, 1u);
             tc_fence_after();
             constexpr uint32_t idS = idesc_f16_f32(kKeys, NQ, 0, 0);
-            constexpr uint32_t idO = idesc_f16_f32(128, 2 * NQ, 1, 0);
+            constexpr uint32_t idO = idesc_f16_f32(128, C::N2, 1, 1);
             const uint32_t q_base = smem_addr(sm + C::Q_OFF);
             int piece = 0;
             auto issue_s = [&](int i) {
@@ -354,12 +397,11 @@ attn_sw_kernel(const __grid_constant__ SwArgs a, const __grid_constant__ SwMaps 
                     wait(bar(C::B_FULL + st), (piece / C::R) & 1);
                     tc_fence_after();
                     const uint32_t vb = smem_addr(sm + C::RING_OFF + st * kStage);
-                    const uint32_t d = tbase + C::TM_O + h * 2 * NQ;
+                    const uint32_t d = tbase + C::TM_O + h * C::N2;
 #pragma unroll
                     for (int ks = 0; ks < 8; ++ks)               // 16 keys per MMA
-                        mma_ss(d, sdesc_sw128(vb + ks * 2048, kBox, 1024),
-                               sdesc_sw128(pb + (ks >> 2) * C::P_BOX + (ks & 3) * 32, 16, 1024), idO,
-                               (i > 0 || ks > 0) ? 1u : 0u);
+                        mma_ss(d, sdesc_sw128(vb + ks * 2048, kBox, 1024), sdesc_sw128(pb + ks * 2048, kBox, 1024),
+                               idO, (i > 0 || ks > 0) ? 1u : 0u);
                     mma_commit(bar(C::B_EMPTY + st));
                     ++piece;
                 }
@@ -379,119 +421,201 @@ attn_sw_kernel(const __grid_constant__ SwArgs a, const __grid_constant__ SwMaps 
             if (!mbar_wait(bar(C::B_MMADONE), 0, limit)) record_timeout(a.status, 1u);
         }
     } else {
-        // ---- softmax: thread = key k of the tile (S^T lane) ------------------
-        const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
-        const int k = warp * 32 + lane;
-        // token of each query row, four bytes per word
-        uint32_t tokp[NQ / 4];
+        // ---- softmax: thread = (key k of the tile, row half rh) ----------------
+        const int qd = warp & 3, rh = warp >> 2;
+        const uint32_t lane_base = (uint32_t)(qd * 32) << 16;
+        const int k = qd * 32 + lane;
+        const int r0 = rh * RH;                          // this thread's rows [r0, r0 + RH)
+        if (a.rope_in_kernel) {
+            // the f16 Q tile from the f32 rows, with qkv_post's arithmetic (the
+            // same device routines, so the bits equal fr_qkv_post's rows): one
+            // cos/sin per (token, pair), shared by the token's heads; rows >= M
+            // are zero
+            RopeTable& stb = *reinterpret_cast<RopeTable*>(sm + C::AUX_OFF + C::AUX_TB);
+            for (int c = tid; c < HD / 2; c += kSmaxThreads) {
+                stb.turns[c] = tb.turns[c];
+                stb.mix[c] = tb.mix[c];
+                stb.ff[c] = tb.ff[c];
+            }
+            if (tid == 0) {
+                stb.mscale = tb.mscale;
+                stb.q_scale = tb.q_scale;
+                stb.theta_scale = tb.theta_scale;
+                stb.freq_scale = tb.freq_scale;
+                stb.half = tb.half;
+                stb.n_dims = tb.n_dims;
+                stb.mode = tb.mode;
+                stb.yarn = tb.yarn;
+            }
+            asm volatile("griddepcontrol.wait;" ::: "memory");     // pos may come from the grid before
+            unsigned char* sQ = sm + C::Q_OFF;
+            for (int i = tid; i < (NQ - a.M) * (HD / 8); i += kSmaxThreads) {      // zero rows [M, NQ)
+                const int r = a.M + i / (HD / 8), ch = i % (HD / 8);
+                *reinterpret_cast<uint4*>(sQ + (ch >> 3) * C::Q_BOX + r * 128 + ((ch & 7) << 4)) =
+                    make_uint4(0u, 0u, 0u, 0u);
+            }
+            softmax_bar_sync();
+            wait(bar(C::B_QF32), 0);
+            const float* q32 = reinterpret_cast<const float*>(sm + C::P_OFF);   // [M][HD]
+            const float q_scale = stb.q_scale;
+            for (int it = tid; it < a.n_tok * (HD / 2); it += kSmaxThreads) {
+                const int t = it / (HD / 2), c = it - t * (HD / 2);
+                int d0, d1;
+                rope_slot_dims(c, stb, d0, d1);
+                const bool rot = c < stb.half;
+                float cs = 0.f, sn = 0.f;
+                if (rot) rope_cs_tab(__ldg(a.pos + t), c, stb, cs, sn);
+                for (int h = 0; h < a.n_head; ++h) {
+                    const int r = t * a.n_head + h;
+                    const float x0 = q32[r * HD + d0], x1 = q32[r * HD + d1];
+                    const float y0 = rot ? rope_lo(x0, x1, cs, sn, q_scale) : __fmul_rn(x0, q_scale);
+                    const float y1 = rot ? rope_hi(x0, x1, cs, sn, q_scale) : __fmul_rn(x1, q_scale);
+                    unsigned char* row = sQ + r * 128;
+                    *reinterpret_cast<__half*>(row + (d0 >> 6) * C::Q_BOX + ((((d0 & 63) >> 3) ^ (r & 7)) << 4) +
+                                               (d0 & 7) * 2) = __float2half_rn(y0);
+                    *reinterpret_cast<__half*>(row + (d1 >> 6) * C::Q_BOX + ((((d1 & 63) >> 3) ^ (r & 7)) << 4) +
+                                               (d1 & 7) * 2) = __float2half_rn(y1);
+                }
+            }
+            softmax_bar_sync();                  // every f32 row read: the P buffers are free again
+        }
+        // P^T columns [2NQ, N2) stay zero (the MMA's N is at least 64)
+        if constexpr (2 * NQ < C::N2) {
+            for (int i = tid; i < 2 * kKeys * ((C::N2 - 2 * NQ) / 8); i += kSmaxThreads) {
+                const int buf = i / (kKeys * ((C::N2 - 2 * NQ) / 8));
+                const int rem = i - buf * (kKeys * ((C::N2 - 2 * NQ) / 8));
+                const int kr = rem / ((C::N2 - 2 * NQ) / 8), ch = 2 * NQ / 8 + rem % ((C::N2 - 2 * NQ) / 8);
+                *reinterpret_cast<uint4*>(sm + C::P_OFF + buf * C::P_BYTES + kr * 128 + ((ch ^ (kr & 7)) << 4)) =
+                    make_uint4(0u, 0u, 0u, 0u);
+            }
+        }
+        fence_proxy_async_cta();                 // the Q tile and the zeros are read by the tensor cores
+        if (a.rope_in_kernel) mbar_arrive(bar(C::B_QFULL));
+
+        // token of each of this thread's rows, four bytes per word
+        uint32_t tokp[(RH + 3) / 4];
 #pragma unroll
-        for (int w4 = 0; w4 < NQ / 4; ++w4) {
+        for (int w4 = 0; w4 < (RH + 3) / 4; ++w4) {
             uint32_t pk = 0;
 #pragma unroll
-            for (int u = 0; u < 4; ++u) pk |= (uint32_t)min((w4 * 4 + u) / a.n_head, a.n_tok - 1) << (8 * u);
+            for (int u = 0; u < 4; ++u) pk |= (uint32_t)min((r0 + w4 * 4 + u) / a.n_head, a.n_tok - 1) << (8 * u);
             tokp[w4] = pk;
         }
-        const int rb = rs_row<CH>(lane);
-        const bool writer = (lane & (32 / CH - 1)) == 0;
+        const int rb = rs_row<RH>(lane);
+        const bool writer = (lane & (32 / RH - 1)) == 0;
         const float kq = a.kq_log2;
-        float l_part[NQ];
+        float l_part[RH], mref[RH];
 #pragma unroll
-        for (int r = 0; r < NQ; ++r) l_part[r] = 0.f;
+        for (int u = 0; u < RH; ++u) {
+            l_part[u] = 0.f;
+            mref[u] = -INFINITY;
+        }
         for (int i = 0; i < n_my; ++i) {
             wait(bar(C::B_SFULL + (i & 1)), (i >> 1) & 1);
             tc_fence_after();
-            float x[NQ];
-            tmem_ld_cols<NQ>(tbase + lane_base + C::TM_S + (i & 1) * NQ, x);
+            float x[RH];
+            tmem_ld_cols<RH>(tbase + lane_base + C::TM_S + (i & 1) * NQ + r0, x);
             tmem_wait_ld();
-            const bool key_ok = (t0 + i) * kKeys + k < a.n_kv;
+            const bool key_ok = k_begin + i * kKeys + k < k_end;
             if (a.has_mask) {
                 wait(bar(C::B_MFULL + i % C::MS), (i / C::MS) & 1);
                 const unsigned char* mk = sm + C::M_OFF + (i % C::MS) * C::MASK_BYTES + (k >> 6) * C::MASK_BOX +
                                           (k & 63) * 2;
 #pragma unroll
-                for (int r = 0; r < NQ; ++r) {
-                    const int t = (tokp[r >> 2] >> (8 * (r & 3))) & 0xff;
+                for (int u = 0; u < RH; ++u) {
+                    const int t = (tokp[u >> 2] >> (8 * (u & 3))) & 0xff;
                     const float mv = __half2float(*reinterpret_cast<const __half*>(mk + t * 128));
-                    x[r] = fmaf(mv, kLog2e, x[r] * kq);
+                    x[u] = fmaf(mv, kLog2e, x[u] * kq);
                 }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar(C::B_MEMPTY + i % C::MS));
             } else {
 #pragma unroll
-                for (int r = 0; r < NQ; ++r) x[r] *= kq;
+                for (int u = 0; u < RH; ++u) x[u] *= kq;
             }
+            bool over = false;
 #pragma unroll
-            for (int r = 0; r < NQ; ++r)
-                if (!key_ok || r >= a.M) x[r] = -INFINITY;
-            // row maxima of this tile: the warp's 32 keys, then the four warps
-#pragma unroll
-            for (int c0 = 0; c0 < NQ; c0 += CH) {
-                float v[CH];
-#pragma unroll
-                for (int u = 0; u < CH; ++u) v[u] = x[c0 + u];
-                ReduceScatter<16, CH, CH, true>::run(v, lane);
-                if (writer) sRed[warp * NQ + c0 + rb] = v[0];
+            for (int u = 0; u < RH; ++u) {
+                if (!key_ok || r0 + u >= a.M) x[u] = -INFINITY;
+                over |= x[u] > mref[u] + kTau;           // -inf + tau = -inf: a first finite score counts
             }
-            softmax_bar_sync();
-            if (tid < NQ) {
-                const float tm = fmaxf(fmaxf(sRed[tid], sRed[NQ + tid]), fmaxf(sRed[2 * NQ + tid], sRed[3 * NQ + tid]));
-                const float m_old = sM[tid];
-                float m_new = m_old;
-                if (tm > m_old + kTau || (m_old == -INFINITY && tm > -INFINITY)) m_new = fmaxf(tm, m_old);
-                const bool grow = m_old != -INFINITY && m_new != m_old;
-                sA[tid] = grow ? ex2(m_old - m_new) : 1.f;
-                sM[tid] = m_new;
-                if (grow) sFlag[i & 1] = 1;
-            }
-            if (tid == 0) sFlag[(i + 1) & 1] = 0;        // read next in tile i + 1
-            softmax_bar_sync();
-            if (sFlag[i & 1]) {
-                // some row's reference grew: rescale this thread's partial sums,
-                // and the O^T columns of its TMEM lane (head dim k of each half)
-                // once PV_{i-1} is complete
+            // the row references change only when some score exceeds its row's
+            // reference by more than 2^8: then the row maxima of this tile are
+            // reduced (warp shuffles, then the four lane quadrants), and every
+            // row whose maximum exceeded its reference takes it
+            if (softmax_bar_any(over)) {
+                float v[RH];
 #pragma unroll
-                for (int r = 0; r < NQ; r += 4) {
-                    const float4 al = *reinterpret_cast<const float4*>(sA + r);
-                    l_part[r] *= al.x;
-                    l_part[r + 1] *= al.y;
-                    l_part[r + 2] *= al.z;
-                    l_part[r + 3] *= al.w;
+                for (int u = 0; u < RH; ++u) v[u] = x[u];
+                ReduceScatter<16, RH, RH, true>::run(v, lane);
+                if (writer) sRed[qd * NQ + r0 + rb] = v[0];
+                softmax_bar_sync();
+                if (tid < NQ) {
+                    const float tm = fmaxf(fmaxf(sRed[tid], sRed[NQ + tid]), fmaxf(sRed[2 * NQ + tid], sRed[3 * NQ + tid]));
+                    const float m_old = sM[tid];
+                    float m_new = m_old;
+                    if (tm > m_old + kTau) m_new = fmaxf(tm, m_old);
+                    const bool grow = m_old != -INFINITY && m_new != m_old;
+                    sA[tid] = grow ? ex2(m_old - m_new) : 1.f;
+                    sM[tid] = m_new;
+                    if (grow) sFlag[0] = 1;
                 }
-                if (i > 0) {
-                    wait(bar(C::B_ODONE), (i - 1) & 1);
-                    tc_fence_after();
+                softmax_bar_sync();
+                const bool grew = sFlag[0] != 0;
+#pragma unroll
+                for (int u = 0; u < RH; ++u) mref[u] = sM[r0 + u];
+                if (grew) {
+                    // rescale this thread's partial sums, and the O^T columns of
+                    // its rows in its TMEM lane (head dim k of each half) once
+                    // PV_{i-1} is complete
+#pragma unroll
+                    for (int u = 0; u < RH; ++u) l_part[u] *= sA[r0 + u];
+                    if (i > 0) {
+                        wait(bar(C::B_ODONE), (i - 1) & 1);
+                        tc_fence_after();
 #pragma unroll 1
-                    for (int c = 0; c < C::HALVES * 2 * NQ; c += 32) {
-                        uint32_t o[32];
-                        tmem_ld_x32(tbase + lane_base + C::TM_O + c, o);
-                        tmem_wait_ld();
+                        for (int h = 0; h < C::HALVES; ++h)
+#pragma unroll 1
+                            for (int lo = 0; lo < 2; ++lo)
+#pragma unroll 1
+                                for (int c8 = 0; c8 < RH; c8 += 8) {
+                                    const uint32_t col = tbase + lane_base + C::TM_O + h * C::N2 + lo * NQ + r0 + c8;
+                                    float o[8];
+                                    tmem_ld_x8(col, reinterpret_cast<uint32_t*>(o));
+                                    tmem_wait_ld();
 #pragma unroll
-                        for (int u = 0; u < 32; ++u)
-                            o[u] = __float_as_uint(__uint_as_float(o[u]) * sA[(c + u) % NQ]);
-                        tmem_st_x32(tbase + lane_base + C::TM_O + c, o);
+                                    for (int u = 0; u < 8; ++u) o[u] *= sA[r0 + c8 + u];
+                                    tmem_st_x8(col, reinterpret_cast<const uint32_t*>(o));
+                                }
+                        tmem_wait_st();
                     }
-                    tmem_wait_st();
                 }
+                softmax_bar_sync();                      // everyone has read sFlag and sM
+                if (tid == 0) sFlag[0] = 0;
             }
-            // P = 2^(x - m) as f16 P_hi and P_lo, key k of rows r and NQ + r of
-            // the K-major (128-byte swizzled) B operand of tile i
-            unsigned char* pbuf = sm + C::P_OFF + (i & 1) * C::P_BYTES + (k >> 6) * C::P_BOX;
-            const int kc = (k & 63) >> 3, kb2 = (k & 7) * 2;
+            // P = 2^(x - m) as f16 P_hi and P_lo: row k of the MN-major B operand
+            // P^T, columns r (P_hi) and NQ + r (P_lo), 16-byte chunks
+            unsigned char* prow = sm + C::P_OFF + (i & 1) * C::P_BYTES + k * 128;
 #pragma unroll
-            for (int r = 0; r < NQ; r += 4) {
-                const float4 m4 = *reinterpret_cast<const float4*>(sM + r);
-                const float mm[4] = {m4.x, m4.y, m4.z, m4.w};
+            for (int c8 = 0; c8 < RH; c8 += 8) {
+                uint32_t hw[4], lw[4];
 #pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    const int rr = r + u, rl = NQ + r + u;
-                    const float msub = mm[u] == -INFINITY ? 0.f : mm[u];
-                    const float p = ex2(x[rr] - msub);
-                    l_part[rr] += p;
-                    const __half hi = __float2half_rn(p);
-                    const __half lo = __float2half_rn(p - __half2float(hi));
-                    *reinterpret_cast<__half*>(pbuf + rr * 128 + ((kc ^ (rr & 7)) << 4) + kb2) = hi;
-                    *reinterpret_cast<__half*>(pbuf + rl * 128 + ((kc ^ (rl & 7)) << 4) + kb2) = lo;
+                for (int u2 = 0; u2 < 4; ++u2) {
+                    const int u = c8 + 2 * u2;
+                    const float m0 = mref[u] == -INFINITY ? 0.f : mref[u];
+                    const float m1 = mref[u + 1] == -INFINITY ? 0.f : mref[u + 1];
+                    const float p0 = ex2(x[u] - m0), p1 = ex2(x[u + 1] - m1);
+                    l_part[u] += p0;
+                    l_part[u + 1] += p1;
+                    hw[u2] = pack_half2(p0, p1);
+                    const float2 hf = __half22float2(*reinterpret_cast<const __half2*>(&hw[u2]));
+                    lw[u2] = pack_half2(p0 - hf.x, p1 - hf.y);
                 }
+                const int ch_hi = (r0 + c8) >> 3, ch_lo = (NQ + r0 + c8) >> 3;     // 16-byte chunks of 8 columns
+                unsigned char* bh = prow + (ch_hi >> 3) * kBox;
+                unsigned char* bl = prow + (ch_lo >> 3) * kBox;
+                *reinterpret_cast<uint4*>(bh + (((ch_hi & 7) ^ (k & 7)) << 4)) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+                *reinterpret_cast<uint4*>(bl + (((ch_lo & 7) ^ (k & 7)) << 4)) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
             }
             fence_proxy_async_cta();            // the tile is read by the tensor cores
             tc_fence_before();
@@ -503,50 +627,35 @@ attn_sw_kernel(const __grid_constant__ SwArgs a, const __grid_constant__ SwMaps 
         if (!mbar_wait(bar(C::B_MMADONE), 0, limit)) record_timeout(a.status, 1u);
         tc_fence_after();
         // row sums: this thread's partials over the warp's keys, then the four
-        // warps, always in the same order
-#pragma unroll
-        for (int c0 = 0; c0 < NQ; c0 += CH) {
-            float v[CH];
-#pragma unroll
-            for (int u = 0; u < CH; ++u) v[u] = l_part[c0 + u];
-            ReduceScatter<16, CH, CH, false>::run(v, lane);
-            if (writer) sRed[warp * NQ + c0 + rb] = v[0];
-        }
+        // lane quadrants, always in the same order
+        ReduceScatter<16, RH, RH, false>::run(l_part, lane);
+        if (writer) sRed[qd * NQ + r0 + rb] = l_part[0];
         softmax_bar_sync();
         if (tid < NQ) sL[tid] = (sRed[tid] + sRed[NQ + tid]) + (sRed[2 * NQ + tid] + sRed[3 * NQ + tid]);
         softmax_bar_sync();
-        // ---- epilogue: O = O_hi + O_lo; this thread's lane is head dim k of each half
+        // ---- epilogue: O = O_hi + O_lo; this thread's lane is head dim k of
+        // each half, its rows [r0, r0 + RH)
         const int rows = a.M;
         const bool single = a.splits == 1;
+        constexpr int EC = RH < 16 ? RH : 16;            // columns per TMEM read
 #pragma unroll 1
         for (int h = 0; h < C::HALVES; ++h) {
             const int d = h * 128 + k;
-            const uint32_t col0 = tbase + lane_base + C::TM_O + h * 2 * NQ;
 #pragma unroll 1
-            for (int c0 = 0; c0 < NQ; c0 += CH) {
-                float hi[CH], lo[CH];
+            for (int c0 = 0; c0 < RH; c0 += EC) {
+                const uint32_t col0 = tbase + lane_base + C::TM_O + h * C::N2 + r0 + c0;
+                float hi[EC], lo[EC];
                 if (n_my > 0) {
-                    if constexpr (NQ == 16) {
-                        uint32_t o[32];
-                        tmem_ld_x32(col0, o);
-                        tmem_wait_ld();
-#pragma unroll
-                        for (int u = 0; u < 16; ++u) {
-                            hi[u] = __uint_as_float(o[u]);
-                            lo[u] = __uint_as_float(o[16 + u]);
-                        }
-                    } else {
-                        tmem_ld_x32(col0 + c0, reinterpret_cast<uint32_t*>(hi));
-                        tmem_ld_x32(col0 + NQ + c0, reinterpret_cast<uint32_t*>(lo));
-                        tmem_wait_ld();
-                    }
+                    tmem_ld_cols<EC>(col0, hi);
+                    tmem_ld_cols<EC>(col0 + NQ, lo);
+                    tmem_wait_ld();
                 } else {
 #pragma unroll
-                    for (int u = 0; u < CH; ++u) hi[u] = lo[u] = 0.f;
+                    for (int u = 0; u < EC; ++u) hi[u] = lo[u] = 0.f;
                 }
 #pragma unroll
-                for (int u = 0; u < CH; ++u) {
-                    const int r = c0 + u;
+                for (int u = 0; u < EC; ++u) {
+                    const int r = r0 + c0 + u;
                     if (r < rows) {
                         const float o = hi[u] + lo[u];
                         if (single) {
@@ -596,7 +705,7 @@ static fr_status launch(const SwLaunch& L, cudaStream_t stream) {
     const SwArgs& a = L.args;
     if (!tc::encode_f16_2d(&mp.k, L.k, HD, a.n_kv, L.k_rs, 64, kKeys, true)) return FR_ERR_CUDA;
     if (!tc::encode_f16_2d(&mp.v, L.v, HD, a.n_kv, L.v_rs, 64, kKeys, true)) return FR_ERR_CUDA;
-    if (!tc::encode_f16_2d(&mp.q16, L.q16, HD, a.M, HD, 64, NQ, true)) return FR_ERR_CUDA;
+    if (!a.rope_in_kernel && !tc::encode_f16_2d(&mp.q16, L.q16, HD, a.M, HD, 64, NQ, true)) return FR_ERR_CUDA;
     if (a.has_mask &&
         !tc::encode_f16_2d(&mp.mask, L.mask, a.n_kv, a.n_tok, L.m_rs, 64,
                            (uint32_t)(a.n_tok < kMaskWin ? a.n_tok : kMaskWin), false))
@@ -612,7 +721,7 @@ static fr_status launch(const SwLaunch& L, cudaStream_t stream) {
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = L.pdl ? 1 : 0;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, attn_sw_kernel<HD, NQ>, a, mp);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, attn_sw_kernel<HD, NQ>, a, mp, L.tb);
     return e == cudaSuccess ? FR_OK : FR_ERR_CUDA;
 }
 

@@ -522,22 +522,25 @@ static TcPlan choose_tc_plan(int M, int hd, int n_kv, int num_sms, const fr_attn
 
 static size_t sw_split_bytes(int M, int hd) { return (size_t)M * (hd * sizeof(float) + sizeof(float2)); }
 
+// Splits cover equal key ranges in multiples of 16 keys (so every SM gets a
+// share even when the 128-key tiles do not divide evenly); a split's last tile
+// may be short, its keys past the range masked.
 struct SwPlan {
-    int n_tiles, splits, tiles_per_split;
+    int splits, keys_per_split;
 };
 
 static SwPlan make_sw_plan(int M, int hd, int n_kv, int num_sms, int force_splits, size_t ws_bytes) {
     SwPlan p;
-    p.n_tiles = (n_kv + 127) / 128;
+    const int units = (n_kv + 15) / 16;
     int S = force_splits > 0 ? force_splits : num_sms;
-    S = max(1, min(S, min(p.n_tiles, min(num_sms, tc::kMaxMergeSplits))));
+    S = max(1, min(S, min(units, min(num_sms, tc::kMaxMergeSplits))));
     if (S > 1) {
         const size_t fixed = kWsHeader + tc_q16_bytes(M, hd);
         const size_t fit = ws_bytes > fixed ? (ws_bytes - fixed) / sw_split_bytes(M, hd) : 0;
         if ((size_t)S > fit) S = fit > 1 ? (int)fit : 1;
     }
-    p.tiles_per_split = (p.n_tiles + S - 1) / S;
-    p.splits = (p.n_tiles + p.tiles_per_split - 1) / p.tiles_per_split;
+    p.keys_per_split = (units + S - 1) / S * 16;
+    p.splits = (n_kv + p.keys_per_split - 1) / p.keys_per_split;
     return p;
 }
 
@@ -619,10 +622,12 @@ static fr_status decode_attn_impl(const uint16_t* q16, const float* q, int64_t q
         if (q16) {
             L.q16 = q16;
         } else {
-            const fr_status st = launch_qkv_post(q, q_tok_stride, pos, n_tok, n_head, hd, tb,
-                                                 reinterpret_cast<uint16_t*>(qslot), nullptr, stream);
-            if (st != FR_OK) return st;
-            L.q16 = qslot;
+            // qkv_post inside the attention kernel: one launch per call
+            a.rope_in_kernel = 1;
+            a.q = q;
+            a.q_tok_stride = q_tok_stride;
+            a.pos = pos;
+            L.tb = tb;
             L.pdl = true;
         }
         a.out = out;
@@ -634,8 +639,7 @@ static fr_status decode_attn_impl(const uint16_t* q16, const float* q, int64_t q
         a.n_head = n_head;
         a.M = M;
         a.n_kv = n_kv;
-        a.n_tiles = p.n_tiles;
-        a.tiles_per_split = p.tiles_per_split;
+        a.keys_per_split = p.keys_per_split;
         a.splits = p.splits;
         a.rstride = M;
         a.early_dep = 1;                     // at most one CTA per SM: one wave
@@ -807,7 +811,8 @@ extern "C" fr_status fr_decode_attn_plan(int n_tok, int n_head, int hd, int n_kv
         plan->cluster = 1;
         plan->merge_kernel = 0;
     }
-    plan->launches = (fused_qkv_post && o.engine == 0 ? 1 : 0) + 1 + plan->merge_kernel;
+    // the keys-on-M kernel ropes the Q rows itself: no separate qkv_post launch
+    plan->launches = (fused_qkv_post && o.engine == 0 && !plan->keys_on_m ? 1 : 0) + 1 + plan->merge_kernel;
     return FR_OK;
 }
 
