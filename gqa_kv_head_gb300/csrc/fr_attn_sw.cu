@@ -101,7 +101,8 @@ struct Cfg {
     static constexpr int AUX_A = AUX_M + NQ * 4;
     static constexpr int AUX_L = AUX_A + NQ * 4;
     static constexpr int AUX_FLAG = AUX_L + NQ * 4;
-    static constexpr int AUX_TB = (AUX_FLAG + 16 + 15) / 16 * 16;
+    static constexpr int AUX_POS = AUX_FLAG + 16;    // [kMaskWin] token positions (fused call)
+    static constexpr int AUX_TB = (AUX_POS + kMaskWin * 4 + 15) / 16 * 16;
     static_assert(AUX_TB + (int)sizeof(RopeTable) <= AUX, "aux");
     static constexpr int B_FULL = 0, B_EMPTY = R, B_MFULL = 2 * R, B_MEMPTY = 2 * R + MS,
                          B_SFULL = 2 * (R + MS), B_PFULL = B_SFULL + 2, B_ODONE = B_SFULL + 4,
@@ -309,6 +310,24 @@ attn_sw_kernel(const __grid_constant__ SwArgs a, const __grid_constant__ SwMaps 
                 tma_load_2d(dst, &mp.mask, k_begin + i * kKeys, 0, bar(C::B_MFULL + st));
                 tma_load_2d(dst + C::MASK_BOX, &mp.mask, k_begin + i * kKeys + 64, 0, bar(C::B_MFULL + st));
             };
+            // While the grid ahead finishes, the first inputs are prefetched into
+            // L2 (a prefetch returns no data, so it may precede the wait below):
+            // the Q rows, the first mask tiles and the first ring's K/V stages.
+            if (a.rope_in_kernel)
+                for (int t = 0; t < a.n_tok; ++t)
+                    bulk_prefetch_l2(a.q + (int64_t)t * a.q_tok_stride, (uint32_t)(a.n_head * HD * 4));
+            for (int i = 0; i < min(C::MS, n_masks); ++i) {
+                tma_prefetch_2d(&mp.mask, k_begin + i * kKeys, 0);
+                tma_prefetch_2d(&mp.mask, k_begin + i * kKeys + 64, 0);
+            }
+            for (int p = 0; p < min(C::R, n_pieces); ++p) {
+                const int u = p / C::HALVES, h = p - u * C::HALVES;
+                const bool is_v = u == n_units - 1 || (u > 0 && !(u & 1));
+                const int tile = u == 0 ? 0 : (u == n_units - 1 ? n_my - 1 : ((u & 1) ? (u + 1) >> 1 : (u >> 1) - 1));
+                const CUtensorMap* m = is_v ? &mp.v : &mp.k;
+                tma_prefetch_2d(m, (2 * h) * 64, k_begin + tile * kKeys);
+                tma_prefetch_2d(m, (2 * h + 1) * 64, k_begin + tile * kKeys);
+            }
             // launched as a programmatic dependent: no input is read before the
             // grids ahead of this one on the stream are complete (one of them
             // may have written the KV rows or the Q rows)
@@ -325,9 +344,13 @@ attn_sw_kernel(const __grid_constant__ SwArgs a, const __grid_constant__ SwMaps 
                 for (int b = 0; b < HD / 64; ++b)
                     tma_load_2d(smem_addr(sm + C::Q_OFF + b * C::Q_BOX), &mp.q16, b * 64, 0, bar(C::B_QFULL));
             }
+            // the Q rows and the first mask tiles first, on their own: issued
+            // together with every CTA's first K/V stages they would queue behind
+            // tens of MB of requests, and the first tile needs them
             int np = 0, nm = 0;
-            for (; np < min(C::R, n_pieces); ++np) load_piece(np);
             for (; nm < min(C::MS, n_masks); ++nm) load_mask(nm);
+            if (!mbar_wait(bar(a.rope_in_kernel ? C::B_QF32 : C::B_QFULL), 0, limit)) record_timeout(a.status, 1u);
+            for (; np < min(C::R, n_pieces); ++np) load_piece(np);
             uint64_t t_last = global_ns();
             while (np < n_pieces || nm < n_masks) {
                 bool moved = false;
@@ -448,6 +471,9 @@ attn_sw_kernel(const __grid_constant__ SwArgs a, const __grid_constant__ SwMaps 
                 stb.yarn = tb.yarn;
             }
             asm volatile("griddepcontrol.wait;" ::: "memory");     // pos may come from the grid before
+            // the positions now, before the K/V stream starts (the RoPE needs them)
+            int* sPos = reinterpret_cast<int*>(sm + C::AUX_OFF + C::AUX_POS);
+            if (tid < a.n_tok) sPos[tid] = __ldg(a.pos + tid);
             unsigned char* sQ = sm + C::Q_OFF;
             for (int i = tid; i < (NQ - a.M) * (HD / 8); i += kSmaxThreads) {      // zero rows [M, NQ)
                 const int r = a.M + i / (HD / 8), ch = i % (HD / 8);
@@ -458,14 +484,16 @@ attn_sw_kernel(const __grid_constant__ SwArgs a, const __grid_constant__ SwMaps 
             wait(bar(C::B_QF32), 0);
             const float* q32 = reinterpret_cast<const float*>(sm + C::P_OFF);   // [M][HD]
             const float q_scale = stb.q_scale;
-            for (int it = tid; it < a.n_tok * (HD / 2); it += kSmaxThreads) {
-                const int t = it / (HD / 2), c = it - t * (HD / 2);
+            const int groups = (a.n_head + 3) / 4;         // four heads per item, one cos/sin
+            for (int it = tid; it < a.n_tok * groups * (HD / 2); it += kSmaxThreads) {
+                const int c = it % (HD / 2), tg = it / (HD / 2);
+                const int t = tg / groups, h0 = (tg - t * groups) * 4;
                 int d0, d1;
                 rope_slot_dims(c, stb, d0, d1);
                 const bool rot = c < stb.half;
                 float cs = 0.f, sn = 0.f;
-                if (rot) rope_cs_tab(__ldg(a.pos + t), c, stb, cs, sn);
-                for (int h = 0; h < a.n_head; ++h) {
+                if (rot) rope_cs_tab(sPos[t], c, stb, cs, sn);
+                for (int h = h0; h < min(h0 + 4, a.n_head); ++h) {
                     const int r = t * a.n_head + h;
                     const float x0 = q32[r * HD + d0], x1 = q32[r * HD + d1];
                     const float y0 = rot ? rope_lo(x0, x1, cs, sn, q_scale) : __fmul_rn(x0, q_scale);

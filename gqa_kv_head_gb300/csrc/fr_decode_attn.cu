@@ -416,11 +416,17 @@ static size_t tc_merge_workspace_bytes(int M, int hd) {
 static bool sw_shape_ok(int n_tok, int n_head, int hd) {
     return (hd == 128 || hd == 256) && n_tok <= kMaskWin && (int64_t)n_tok * n_head <= sw::kMaxRows;
 }
-static bool use_sw(int n_tok, int n_head, int hd, const fr_attn_opts& o) {
+// The library's choice (measured on GB300, graph replay of fused calls): the
+// keys-on-M kernel wins by 10-25 % at up to 32 query rows and 512 keys or more;
+// at 64 rows its softmax (32 rows per thread) is slower than the 128-row
+// kernel's, and at a few hundred keys the two are within launch noise.
+static constexpr int kSwAutoRows = 32;
+static constexpr int kSwAutoKeys = 512;
+static bool use_sw(int n_tok, int n_head, int hd, int n_kv, const fr_attn_opts& o) {
     if (o.engine != 0 || !sw_shape_ok(n_tok, n_head, hd)) return false;
     if (o.layout == 2) return true;
     if (o.layout == 1 || o.force_cluster != 0 || o.merge_mode == 1) return false;
-    return true;
+    return n_tok * n_head <= kSwAutoRows && n_kv >= kSwAutoKeys;
 }
 
 // Smallest workspace the plan a call with these options takes accepts: the
@@ -429,7 +435,7 @@ static bool use_sw(int n_tok, int n_head, int hd, const fr_attn_opts& o) {
 // plan; the mma.sync engine's needs count for the shapes it takes.
 static size_t workspace_bytes_for(int n_tok, int n_head, int hd, int n_kv, const fr_attn_opts& o) {
     const int M = n_tok * n_head;
-    if (use_sw(n_tok, n_head, hd, o)) return kWsHeader + tc_q16_bytes(M, hd);
+    if (use_sw(n_tok, n_head, hd, n_kv, o)) return kWsHeader + tc_q16_bytes(M, hd);
     const size_t b = tc_workspace_bytes(M, hd);
     if (!decode_shape(n_tok, n_head)) return b;
     const size_t a = v1_workspace_bytes(M, hd, n_kv);
@@ -612,7 +618,7 @@ static fr_status decode_attn_impl(const uint16_t* q16, const float* q, int64_t q
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return FR_ERR_CUDA;
     unsigned char* w = static_cast<unsigned char*>(ws);
 
-    if (use_sw(n_tok, n_head, hd, o)) {
+    if (use_sw(n_tok, n_head, hd, n_kv, o)) {
         const SwPlan p = make_sw_plan(M, hd, n_kv, sms, o.force_splits, ws_bytes);
         sw::SwLaunch L;
         memset(&L, 0, sizeof(L));
@@ -789,7 +795,7 @@ extern "C" fr_status fr_decode_attn_plan(int n_tok, int n_head, int hd, int n_kv
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return FR_ERR_CUDA;
     memset(plan, 0, sizeof(*plan));
     plan->engine = o.engine;
-    if (use_sw(n_tok, n_head, hd, o)) {
+    if (use_sw(n_tok, n_head, hd, n_kv, o)) {
         const SwPlan p = make_sw_plan(M, hd, n_kv, sms, o.force_splits, workspace_bytes);
         plan->row_tiles = 1;
         plan->splits = p.splits;

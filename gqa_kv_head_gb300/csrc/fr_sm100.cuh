@@ -73,6 +73,17 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
         "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
         :: "r"(dst), "l"((uint64_t)map), "r"(x), "r"(y), "r"(bar) : "memory");
 }
+// Prefetch one 2-D box of a tensor into L2 (nothing lands in shared memory,
+// no barrier). L2 is the GPU's point of coherence, so a prefetch never makes a
+// later load return stale data.
+__device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap* map, int x, int y) {
+    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];"
+                 :: "l"((uint64_t)map), "r"(x), "r"(y) : "memory");
+}
+// Prefetch `bytes` (a multiple of 16, 16-byte aligned address) into L2.
+__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" :: "l"(src), "r"(bytes) : "memory");
+}
 // Bulk copy of `bytes` (a multiple of 16) from global to this CTA's shared
 // memory, both addresses 16-byte aligned; the barrier is credited with the bytes.
 __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {

@@ -24,7 +24,10 @@ def _rows(out):
 
 
 def _plan(w, **kw):
-    return fr.decode_attn_plan(w.n_tok, w.n_head, w.hd, w.n_kv, **kw)
+    return fr.decode_attn_plan(w.n_tok, w.n_head, w.hd, w.n_kv, layout=2, **kw)
+
+
+KOM = dict(layout=2)      # the library picks this layout itself for M <= 32 rows and n_kv >= 512
 
 
 @pytest.mark.parametrize("hd", [128, 256])
@@ -35,8 +38,10 @@ def test_row_counts(hd, n_tok, n_head):
                  rope=RopeParams(n_dims=hd, freq_base=10000.0), positions=tuple(range(2999 - n_tok + 1, 3000)),
                  mask_kind="causal", seed=n_tok * 7 + n_head)
     assert _plan(w)["keys_on_m"] == 1
+    auto = fr.decode_attn_plan(w.n_tok, w.n_head, w.hd, w.n_kv)["keys_on_m"]
+    assert auto == (1 if w.M <= 32 else 0)
     d = to_device(w)
-    out = _rows(run_fused(w, d))
+    out = _rows(run_fused(w, d, **KOM))
     ref = oracle_out(w)
     assert_close(out, ref, f"{n_tok}x{n_head} hd {hd}")
     assert_close(_rows(run_fused(w, d, layout=1)), ref, f"{n_tok}x{n_head} hd {hd} query tiles")
@@ -49,7 +54,7 @@ def test_ragged_kv_masks_and_strides(n_kv, hd):
                  rope=RopeParams(n_dims=hd, freq_base=10000.0),
                  positions=tuple(range(n_kv - 1, n_kv + 6)), mask_kind="random5", seed=n_kv % 97)
     d = to_device(w, k_pad=16, mask_pad=8, q_extra_heads=2)
-    assert_close(_rows(run_fused(w, d)), oracle_out(w), w.name)
+    assert_close(_rows(run_fused(w, d, **KOM)), oracle_out(w), w.name)
 
 
 @pytest.mark.parametrize("name", ["sweep:256:1:65536", "sweep:128:8:16384", "sweep:256:4:4096"])
@@ -59,7 +64,7 @@ def test_forced_splits(name, splits):
     d = to_device(w)
     p = _plan(w, splits=splits)
     assert p["keys_on_m"] == 1 and p["splits"] <= max(1, splits)
-    assert_close(_rows(run_fused(w, d, splits=splits)), oracle_out(w), f"{name} splits={splits}")
+    assert_close(_rows(run_fused(w, d, splits=splits, **KOM)), oracle_out(w), f"{name} splits={splits}")
 
 
 def test_workspace_holding_fewer_split_states():
@@ -73,17 +78,17 @@ def test_workspace_holding_fewer_split_states():
     for nbytes in (full, 2 << 20, 300 << 10):
         ws = torch.zeros(max(nbytes, 1 << 20), dtype=torch.uint8, device="cuda")[:nbytes]
         p = _plan(w, workspace_bytes=nbytes)
-        out = _rows(run_fused(w, d, workspace=ws))
+        out = _rows(run_fused(w, d, workspace=ws, **KOM))
         assert_close(out, ref, f"workspace {nbytes}: plan {p}")
     assert _plan(w, workspace_bytes=full)["splits"] > _plan(w, workspace_bytes=2 << 20)["splits"]
 
 
-@pytest.mark.parametrize("name", ["sweep:128:1:65536", "sweep:256:8:4096", "tiny"])
+@pytest.mark.parametrize("name", ["sweep:128:1:65536", "sweep:256:8:4096", "sweep:256:2:1024"])
 def test_fused_equals_two_call_bitwise(name):
     w = make_workload(name)
     d = to_device(w)
-    a = run_fused(w, d)
-    b, _ = run_two_call(w, d)
+    a = run_fused(w, d, **KOM)
+    b, _ = run_two_call(w, d, **KOM)
     torch.cuda.synchronize()
     assert torch.equal(a, b)
 
@@ -93,13 +98,13 @@ def test_repeatable_and_graph_captured():
     d = to_device(w)
     ws = fr.make_workspace(w.n_tok, w.n_head, w.hd, w.n_kv)
     out = torch.empty((w.n_tok, w.n_head, w.hd), dtype=torch.float32, device="cuda")
-    ref = run_fused(w, d, workspace=ws).clone()
-    assert torch.equal(run_fused(w, d, workspace=ws), ref)
+    ref = run_fused(w, d, workspace=ws, **KOM).clone()
+    assert torch.equal(run_fused(w, d, workspace=ws, **KOM), ref)
     s = torch.cuda.Stream()
     s.wait_stream(torch.cuda.current_stream())
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g, stream=s):
-        run_fused(w, d, workspace=ws, out=out, stream=s)
+        run_fused(w, d, workspace=ws, out=out, stream=s, **KOM)
     out.zero_()
     g.replay()
     torch.cuda.synchronize()
@@ -111,11 +116,11 @@ def test_device_timeout_is_reported_and_recoverable():
     w = make_workload("sweep:128:4:4096")
     d = to_device(w)
     ws = fr.make_workspace(w.n_tok, w.n_head, w.hd, w.n_kv)
-    run_fused(w, d, workspace=ws, wait_probe_iters=1000)
+    run_fused(w, d, workspace=ws, wait_probe_iters=1000, **KOM)
     with pytest.raises(fr.FrError) as e:
         fr.workspace_check(ws)
     assert e.value.status == 5
-    out = _rows(run_fused(w, d, workspace=ws))
+    out = _rows(run_fused(w, d, workspace=ws, **KOM))
     fr.workspace_check(ws)
     assert_close(out, oracle_out(w), "after timeout")
 
@@ -124,7 +129,7 @@ def test_fully_masked_token_is_zero():
     w = make_workload("sweep:256:4:4096")
     d = to_device(w)
     d["mask"][2, :] = float("-inf")
-    out = run_fused(w, d)
+    out = run_fused(w, d, **KOM)
     torch.cuda.synchronize()
     assert torch.all(torch.isfinite(out)) and torch.equal(out[2], torch.zeros_like(out[2]))
 
