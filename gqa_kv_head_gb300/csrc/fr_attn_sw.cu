@@ -162,6 +162,11 @@ __device__ __forceinline__ int rs_row(int lane) {
 }
 
 __device__ __forceinline__ void record_timeout(unsigned* status, unsigned bit) { atomicOr(status, bit); }
+__device__ __forceinline__ unsigned ld_acquire_u32(const unsigned* p) {
+    unsigned v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
 
 // Barrier over the softmax warps (named barrier 1).
 __device__ __forceinline__ void softmax_bar_sync() {
@@ -701,6 +706,128 @@ attn_sw_kernel(const __grid_constant__ SwArgs a, const __grid_constant__ SwMaps 
                 n_my > 0 ? make_float2(sM[tid], sL[tid]) : make_float2(-INFINITY, 0.f);
     }
 
+    // ---- the split merge, inside the launch ------------------------------------
+    // Every CTA is resident (cooperative launch, one CTA per SM), so a bounded
+    // grid barrier is safe: once every split's state is stored, CTA b merges
+    // the units (row, 32 columns) b, b + splits, ... Each softmax warp loads
+    // its share of the splits' states for a unit in one round (all loads in
+    // flight), the warps combine through shared memory in a fixed order; with
+    // few splits every warp merges whole units on its own. A wait that gives
+    // up sets the status word and the CTA carries on.
+    if (a.splits > 1) {
+        __syncthreads();                         // this CTA's state is stored
+        if (tid == 0) {
+            unsigned* count = a.barrier;
+            unsigned* gen_w = a.barrier + 1;
+            const unsigned gen = ld_acquire_u32(gen_w);    // it cannot move before this CTA arrives
+            __threadfence();
+            if (atomicAdd(count, 1u) == (unsigned)a.splits - 1u) {
+                *count = 0u;                     // ready for the next call
+                __threadfence();
+                atomicAdd(gen_w, 1u);            // release every CTA
+            } else {
+                const uint64_t t_start = global_ns();
+                while (ld_acquire_u32(gen_w) == gen) {
+                    if (global_ns() - t_start > limit) {
+                        record_timeout(a.status, 4u);
+                        break;
+                    }
+                    __nanosleep(32);
+                }
+            }
+            __threadfence();
+        }
+        __syncthreads();
+        constexpr int kWarpMerge = 16;           // up to this many splits, one warp merges a unit alone
+        if (warp < kSmaxWarps && a.splits <= kWarpMerge) {
+            constexpr int NCH = HD / 32;
+            const int units = a.M * NCH;
+            const int S = a.splits;
+            for (int u = split * kSmaxWarps + warp; u < units; u += S * kSmaxWarps) {
+                const int r = u / NCH, c0 = (u - r * NCH) * 32;
+                float2 ml[kWarpMerge];
+                float ov[kWarpMerge];
+#pragma unroll
+                for (int j = 0; j < kWarpMerge; ++j) {
+                    if (j < S) {
+                        const int64_t row = (int64_t)j * a.rstride + r;
+                        ml[j] = __ldcg(a.part_ml + row);
+                        ov[j] = __ldcg(a.part_o + row * HD + c0 + lane);
+                    } else {
+                        ml[j] = make_float2(-INFINITY, 0.f);
+                        ov[j] = 0.f;
+                    }
+                }
+                float mx = -INFINITY;
+#pragma unroll
+                for (int j = 0; j < kWarpMerge; ++j) mx = fmaxf(mx, ml[j].x);
+                const float ref = mx == -INFINITY ? 0.f : mx;
+                float acc = 0.f, L = 0.f;
+#pragma unroll
+                for (int j = 0; j < kWarpMerge; ++j) {          // split order: deterministic
+                    const float w = ml[j].x == -INFINITY ? 0.f : ex2(ml[j].x - ref);
+                    L = fmaf(w, ml[j].y, L);
+                    acc = fmaf(w, ov[j], acc);
+                }
+                a.out[(int64_t)r * HD + c0 + lane] = L > 0.f ? acc / L : 0.f;
+            }
+        } else if (warp < kSmaxWarps) {
+            constexpr int NCH = HD / 32;
+            constexpr int PW = (tc::kMaxMergeSplits + kSmaxWarps - 1) / kSmaxWarps;   // splits per warp
+            float* sAcc = reinterpret_cast<float*>(sm + C::RING_OFF);          // [8][32] (the ring is idle)
+            float* sMw = sAcc + kSmaxWarps * 32;                             // [8] warp maxima
+            float* sLw = sMw + kSmaxWarps;                                   // [8] weighted sums
+            const int units = a.M * NCH;
+            const int S = a.splits;
+            for (int u = split; u < units; u += S) {
+                const int r = u / NCH, c0 = (u - r * NCH) * 32;
+                float2 ml[PW];
+                float ov[PW];
+#pragma unroll
+                for (int j = 0; j < PW; ++j) {
+                    const int s2 = warp + j * kSmaxWarps;
+                    if (s2 < S) {
+                        const int64_t row = (int64_t)s2 * a.rstride + r;
+                        ml[j] = __ldcg(a.part_ml + row);
+                        ov[j] = __ldcg(a.part_o + row * HD + c0 + lane);
+                    } else {
+                        ml[j] = make_float2(-INFINITY, 0.f);
+                        ov[j] = 0.f;
+                    }
+                }
+                float mw = -INFINITY;
+#pragma unroll
+                for (int j = 0; j < PW; ++j) mw = fmaxf(mw, ml[j].x);
+                if (lane == 0) sMw[warp] = mw;
+                softmax_bar_sync();
+                float mx = -INFINITY;
+#pragma unroll
+                for (int w = 0; w < kSmaxWarps; ++w) mx = fmaxf(mx, sMw[w]);
+                const float ref = mx == -INFINITY ? 0.f : mx;
+                float acc = 0.f, L = 0.f;
+#pragma unroll
+                for (int j = 0; j < PW; ++j) {
+                    const float w = ml[j].x == -INFINITY ? 0.f : ex2(ml[j].x - ref);
+                    L = fmaf(w, ml[j].y, L);
+                    acc = fmaf(w, ov[j], acc);
+                }
+                sAcc[warp * 32 + lane] = acc;
+                if (lane == 0) sLw[warp] = L;
+                softmax_bar_sync();
+                if (warp == 0) {
+                    float sum = 0.f, Lt = 0.f;
+#pragma unroll
+                    for (int w = 0; w < kSmaxWarps; ++w) {              // always the same order
+                        sum += sAcc[w * 32 + lane];
+                        Lt += sLw[w];
+                    }
+                    a.out[(int64_t)r * HD + c0 + lane] = Lt > 0.f ? sum / Lt : 0.f;
+                }
+                softmax_bar_sync();
+            }
+        }
+    }
+
     // ---- teardown ----------------------------------------------------------------
     tc_fence_before();
     __syncthreads();
@@ -744,11 +871,22 @@ static fr_status launch(const SwLaunch& L, cudaStream_t stream) {
     cfg.blockDim = dim3(kThreads, 1, 1);
     cfg.dynamicSmemBytes = Cfg<HD, NQ>::SMEM;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    // several splits merge behind a grid barrier: every CTA must be resident
+    // (cooperative launch; the grid is at most one CTA per SM)
+    cudaLaunchAttribute attr[2];
+    int na = 0;
+    if (a.splits > 1) {
+        attr[na].id = cudaLaunchAttributeCooperative;
+        attr[na].val.cooperative = 1;
+        ++na;
+    }
+    if (L.pdl) {
+        attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[na].val.programmaticStreamSerializationAllowed = 1;
+        ++na;
+    }
     cfg.attrs = attr;
-    cfg.numAttrs = L.pdl ? 1 : 0;
+    cfg.numAttrs = na;
     cudaError_t e = cudaLaunchKernelEx(&cfg, attn_sw_kernel<HD, NQ>, a, mp, L.tb);
     return e == cudaSuccess ? FR_OK : FR_ERR_CUDA;
 }

@@ -37,6 +37,7 @@ constexpr int kThreads = kWarps * 32;
 constexpr int kMaxSplits = 32;
 constexpr size_t kWsHeader = 1024;     // [0,4): status word; [256, 256+4*32): tickets
 constexpr size_t kWsTickets = 256;
+constexpr size_t kWsSwBarrier = 512;   // [512, 520): the keys-on-M kernel's grid barrier (count, generation)
 constexpr float kLog2e = 1.4426950408889634f;
 
 template <int HD>
@@ -417,16 +418,18 @@ static bool sw_shape_ok(int n_tok, int n_head, int hd) {
     return (hd == 128 || hd == 256) && n_tok <= kMaskWin && (int64_t)n_tok * n_head <= sw::kMaxRows;
 }
 // The library's choice (measured on GB300, graph replay of fused calls): the
-// keys-on-M kernel wins by 10-25 % at up to 32 query rows and 512 keys or more;
-// at 64 rows its softmax (32 rows per thread) is slower than the 128-row
-// kernel's, and at a few hundred keys the two are within launch noise.
+// keys-on-M kernel wins by 10-25 % at up to 32 query rows when there are at
+// least 1024 keys and 128 per row; at 64 rows its softmax (32 rows per thread)
+// is slower than the 128-row kernel's, and with fewer keys its few splits
+// leave each merging warp many (row, 32-column) units.
 static constexpr int kSwAutoRows = 32;
-static constexpr int kSwAutoKeys = 512;
+static constexpr int kSwAutoKeys = 1024;
 static bool use_sw(int n_tok, int n_head, int hd, int n_kv, const fr_attn_opts& o) {
     if (o.engine != 0 || !sw_shape_ok(n_tok, n_head, hd)) return false;
     if (o.layout == 2) return true;
     if (o.layout == 1 || o.force_cluster != 0 || o.merge_mode == 1) return false;
-    return n_tok * n_head <= kSwAutoRows && n_kv >= kSwAutoKeys;
+    const int M = n_tok * n_head;
+    return M <= kSwAutoRows && n_kv >= kSwAutoKeys && n_kv >= 128 * M;
 }
 
 // Smallest workspace the plan a call with these options takes accepts: the
@@ -528,9 +531,9 @@ static TcPlan choose_tc_plan(int M, int hd, int n_kv, int num_sms, const fr_attn
 
 static size_t sw_split_bytes(int M, int hd) { return (size_t)M * (hd * sizeof(float) + sizeof(float2)); }
 
-// Splits cover equal key ranges in multiples of 16 keys (so every SM gets a
-// share even when the 128-key tiles do not divide evenly); a split's last tile
-// may be short, its keys past the range masked.
+// Splits cover equal key ranges in multiples of 16 keys, at least 128 (so every
+// SM gets a share even when the 128-key tiles do not divide evenly); a split's
+// last tile may be short, its keys past the range masked.
 struct SwPlan {
     int splits, keys_per_split;
 };
@@ -545,7 +548,9 @@ static SwPlan make_sw_plan(int M, int hd, int n_kv, int num_sms, int force_split
         const size_t fit = ws_bytes > fixed ? (ws_bytes - fixed) / sw_split_bytes(M, hd) : 0;
         if ((size_t)S > fit) S = fit > 1 ? (int)fit : 1;
     }
-    p.keys_per_split = (units + S - 1) / S * 16;
+    // at least one full 128-key tile per split: below that a split still loads
+    // a whole tile and adds a state to merge
+    p.keys_per_split = max((units + S - 1) / S * 16, min(128, units * 16));
     p.splits = (n_kv + p.keys_per_split - 1) / p.keys_per_split;
     return p;
 }
@@ -648,6 +653,7 @@ static fr_status decode_attn_impl(const uint16_t* q16, const float* q, int64_t q
         a.keys_per_split = p.keys_per_split;
         a.splits = p.splits;
         a.rstride = M;
+        a.barrier = reinterpret_cast<unsigned*>(w + kWsSwBarrier);
         a.early_dep = 1;                     // at most one CTA per SM: one wave
         a.kq_log2 = kq_scale * kLog2e;
         a.wait_limit_ns = tc::kWaitLimitNs;
@@ -658,9 +664,7 @@ static fr_status decode_attn_impl(const uint16_t* q16, const float* q, int64_t q
         L.k_rs = k_rs;
         L.v_rs = v_rs;
         L.m_rs = m_rs;
-        const fr_status st = sw::launch_sw(L, hd, stream);
-        if (st != FR_OK || p.splits == 1) return st;
-        return tc::launch_merge(a.part_o, a.part_ml, out, M, p.splits, hd, M, stream);
+        return sw::launch_sw(L, hd, stream);     // the split merge happens inside the launch
     }
 
     if (o.engine == 0) {
@@ -800,7 +804,7 @@ extern "C" fr_status fr_decode_attn_plan(int n_tok, int n_head, int hd, int n_kv
         plan->row_tiles = 1;
         plan->splits = p.splits;
         plan->cluster = 1;
-        plan->merge_kernel = p.splits > 1 ? 1 : 0;
+        plan->merge_kernel = 0;              // merged inside the launch
         plan->keys_on_m = 1;
     } else if (o.engine == 0) {
         bool ok = true;

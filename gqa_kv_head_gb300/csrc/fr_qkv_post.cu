@@ -103,28 +103,6 @@ bool build_rope_table(const fr_rope_params* rp, float q_scale, int hd, RopeTable
     return true;
 }
 
-// The parameter table into shared memory (block-wide; ends with a barrier):
-// indexing the kernel-parameter copy with a per-thread slot would serialise
-// every access.
-__device__ __forceinline__ void copy_rope_table(const RopeTable& tb, RopeTable& stb, int pairs) {
-    for (int c = threadIdx.x; c < pairs; c += blockDim.x) {
-        stb.turns[c] = tb.turns[c];
-        stb.mix[c] = tb.mix[c];
-        stb.ff[c] = tb.ff[c];
-    }
-    if (threadIdx.x == 0) {
-        stb.mscale = tb.mscale;
-        stb.q_scale = tb.q_scale;
-        stb.theta_scale = tb.theta_scale;
-        stb.freq_scale = tb.freq_scale;
-        stb.half = tb.half;
-        stb.n_dims = tb.n_dims;
-        stb.mode = tb.mode;
-        stb.yarn = tb.yarn;
-    }
-    __syncthreads();
-}
-
 // Every query head of a token rotates its pairs by the same angles, so a work
 // item is (token t, slot c, group of kQkvHeads heads): one cos/sin for the
 // group, then the group's pairs loaded together and rotated. Items are
@@ -140,8 +118,10 @@ qkv_post_kernel(const float* __restrict__ q, int64_t q_tok_stride, const int32_t
     // waits for this grid's completion before it reads the rows.
     asm volatile("griddepcontrol.wait;" ::: "memory");
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    __shared__ RopeTable stb;
-    copy_rope_table(tb, stb, HD / 2);
+    // Each item reads its pair's constants straight from the parameter block:
+    // no shared-memory copy and no block barrier, so the table, position and Q
+    // loads of an item all go out at once (the kernel is latency-bound).
+    const RopeTable& stb = tb;
     constexpr int SLOTS = HD / 2;
     const int groups = (n_head + kQkvHeads - 1) / kQkvHeads;
     const int64_t items = (int64_t)n_tok * groups * SLOTS;
@@ -226,8 +206,7 @@ kv_append_kernel(const float* __restrict__ k_new, int64_t k_stride, const float*
                  const __grid_constant__ RopeTable tb) {
     asm volatile("griddepcontrol.wait;" ::: "memory");
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    __shared__ RopeTable stb;                                  // see qkv_post_kernel
-    copy_rope_table(tb, stb, HD / 2);
+    const RopeTable& stb = tb;                                 // see qkv_post_kernel
     constexpr int G = HD / 8;                                  // 8-element groups per row
     const int64_t nK = (int64_t)n_tok * (HD / 2), nV = (int64_t)n_tok * G, nP = pad_rows * G;
     for (int64_t w = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; w < nK + nV + nP;
