@@ -73,16 +73,18 @@ SIGNATURES = {
 _lib = None
 
 
-def library_path():
-    return _build.library_path()
+def library_path(trace=False):
+    return _build.library_path(trace)
 
 
-def load():
-    """The loaded library (ctypes.CDLL) with argument types declared."""
+def load(trace=False):
+    """The loaded library (ctypes.CDLL) with argument types declared. The first
+    call decides which build the process uses: trace=True loads the
+    timeline-instrumented variant (gqa_kv_head_gb300.trace)."""
     global _lib
     if _lib is not None:
         return _lib
-    path = library_path()
+    path = library_path(trace)
     if not os.path.exists(path):
         raise RuntimeError(f"{path} is missing: build it with gqa_kv_head_gb300.build.build() "
                            "(needs nvcc); this package has no non-CUDA fallback")

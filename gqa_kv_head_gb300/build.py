@@ -25,8 +25,11 @@ FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", 
          "--expt-relaxed-constexpr"]
 
 
-def library_path():
-    return os.path.join(BUILD, LIB_NAME)
+TRACE_BUILD = os.path.join(HERE, "_build_trace")
+
+
+def library_path(trace=False):
+    return os.path.join(TRACE_BUILD if trace else BUILD, LIB_NAME)
 
 
 def _nvcc():
@@ -45,24 +48,29 @@ def _deps():
         glob.glob(os.path.join(INCLUDE, "*.h")) + [os.path.abspath(__file__)]
 
 
-def is_stale():
-    lib = library_path()
+def is_stale(trace=False):
+    lib = library_path(trace)
     if not os.path.exists(lib):
         return True
     t = os.path.getmtime(lib)
     return any(os.path.getmtime(d) > t for d in _deps())
 
 
-def build(force=False, verbose=False, ptxas_verbose=False):
-    """Compile and link if any source is newer than the library. Returns its path."""
-    if not force and not is_stale():
-        return library_path()
-    os.makedirs(BUILD, exist_ok=True)
+def build(force=False, verbose=False, ptxas_verbose=False, trace=False):
+    """Compile and link if any source is newer than the library. Returns its path.
+    trace=True builds the timeline-instrumented variant (FR_TRACE) into its own
+    directory; the library itself never has it."""
+    if not force and not is_stale(trace):
+        return library_path(trace)
+    out_dir = TRACE_BUILD if trace else BUILD
+    os.makedirs(out_dir, exist_ok=True)
     nvcc = _nvcc()
     extra = ["-Xptxas", "-v"] if ptxas_verbose else []
+    if trace:
+        extra = extra + ["-DFR_TRACE"]
 
     def compile_one(src):
-        obj = os.path.join(BUILD, os.path.basename(src)[:-3] + ".o")
+        obj = os.path.join(out_dir, os.path.basename(src)[:-3] + ".o")
         cmd = [nvcc, *ARCH, *FLAGS, *extra, "-I", INCLUDE, "-I", CSRC, "-c", src, "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
@@ -76,13 +84,13 @@ def build(force=False, verbose=False, ptxas_verbose=False):
         for _, log in results:
             if log:
                 print(log)
-    tmp = library_path() + ".tmp"
+    tmp = library_path(trace) + ".tmp"
     cmd = [nvcc, *ARCH, "-shared", "-o", tmp, *objs]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, library_path())
-    return library_path()
+    os.replace(tmp, library_path(trace))
+    return library_path(trace)
 
 
 if __name__ == "__main__":

@@ -80,7 +80,7 @@ struct SwArgs {
     int keys_per_split;       // a multiple of 16; split s reads keys [s*kps, min(n_kv, (s+1)*kps))
     int splits;
     int rstride;              // rows per split block of part_o / part_ml (= M)
-    unsigned* barrier;        // [2]: arrival count, generation (grid barrier before the merge)
+    unsigned* barrier;        // [2]: arrival and departure counts (grid barrier before the merge)
     int early_dep;            // 1: the grid is one wave; a dependent launch may start after set-up
     float kq_log2;
     uint64_t wait_limit_ns;

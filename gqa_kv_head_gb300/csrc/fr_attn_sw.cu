@@ -53,6 +53,25 @@ namespace sw {
 
 using namespace sm100;
 
+// Timeline instrumentation (compile-time option, off in the library): with
+// FR_TRACE defined, CTA b writes global-timer stamps into 64 slots at
+// workspace + FR_TRACE_OFFSET + 512 b (gqa_kv_head_gb300.trace builds that
+// variant into its own library and prints the timeline).
+#ifdef FR_TRACE
+#ifndef FR_TRACE_OFFSET
+#define FR_TRACE_OFFSET (32u << 20)
+#endif
+#define FR_STAMP(i)                                                                                         \
+    do {                                                                                                    \
+        reinterpret_cast<unsigned long long*>(reinterpret_cast<unsigned char*>(a.status) + FR_TRACE_OFFSET)  \
+            [blockIdx.x * 64 + (i)] = global_ns();                                                          \
+    } while (0)
+#else
+#define FR_STAMP(i) \
+    do {            \
+    } while (0)
+#endif
+
 constexpr int kKeys = 128;               // keys per KV tile = the MMA's M
 constexpr int kSmaxWarps = 8;            // two per TMEM lane quadrant
 constexpr int kSmaxThreads = kSmaxWarps * 32;
@@ -162,6 +181,9 @@ __device__ __forceinline__ int rs_row(int lane) {
 }
 
 __device__ __forceinline__ void record_timeout(unsigned* status, unsigned bit) { atomicOr(status, bit); }
+__device__ __forceinline__ void red_release_add_u32(unsigned* p, unsigned v) {
+    asm volatile("red.release.gpu.global.add.u32 [%0], %1;" :: "l"(p), "r"(v) : "memory");
+}
 __device__ __forceinline__ unsigned ld_acquire_u32(const unsigned* p) {
     unsigned v;
     asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
@@ -269,6 +291,7 @@ attn_sw_kernel(const __grid_constant__ SwArgs a, const __grid_constant__ SwMaps 
     __syncthreads();
     tc_fence_after();
     const uint32_t tbase = *sTmemBase;
+    if (tid == 0) FR_STAMP(0);                   // set-up done
     // a dependent grid (the merge kernel, or the next call) may be scheduled
     // now; it waits for this grid's completion before reading what this grid
     // writes. Only when this grid is one wave.
@@ -337,6 +360,7 @@ attn_sw_kernel(const __grid_constant__ SwArgs a, const __grid_constant__ SwMaps 
             // grids ahead of this one on the stream are complete (one of them
             // may have written the KV rows or the Q rows)
             asm volatile("griddepcontrol.wait;" ::: "memory");
+            FR_STAMP(4);                         // the grids ahead are complete
             if (a.rope_in_kernel) {
                 // the f32 Q rows, one bulk copy per token (its n_head rows are contiguous)
                 const uint32_t row_bytes = (uint32_t)(a.n_head * HD * 4);
@@ -351,7 +375,8 @@ attn_sw_kernel(const __grid_constant__ SwArgs a, const __grid_constant__ SwMaps 
             }
             // the Q rows and the first mask tiles first, on their own: issued
             // together with every CTA's first K/V stages they would queue behind
-            // tens of MB of requests, and the first tile needs them
+            // tens of MB of requests, and the first tile needs them (issuing the
+            // first K tile with them measured no faster)
             int np = 0, nm = 0;
             for (; nm < min(C::MS, n_masks); ++nm) load_mask(nm);
             if (!mbar_wait(bar(a.rope_in_kernel ? C::B_QF32 : C::B_QFULL), 0, limit)) record_timeout(a.status, 1u);
@@ -392,6 +417,7 @@ attn_sw_kernel(const __grid_constant__ SwArgs a, const __grid_constant__ SwMaps 
     } else if (warp == kMmaWarp) {
         if (lane == 0) {
             if (!mbar_wait(bar(C::B_QFULL), 0, limit)) record_timeout(a.status, 1u);
+            FR_STAMP(3);                         // the Q tile is in place
             tc_fence_after();
             constexpr uint32_t idS = idesc_f16_f32(kKeys, NQ, 0, 0);
             constexpr uint32_t idO = idesc_f16_f32(128, C::N2, 1, 1);
@@ -415,6 +441,7 @@ attn_sw_kernel(const __grid_constant__ SwArgs a, const __grid_constant__ SwMaps 
                     ++piece;
                 }
                 mma_commit(bar(C::B_SFULL + (i & 1)));
+                if (i < 12) FR_STAMP(8 + 4 * i + 2);     // S_i issued
             };
             auto issue_pv = [&](int i) {
                 wait(bar(C::B_PFULL + (i & 1)), (i >> 1) & 1);
@@ -434,6 +461,7 @@ attn_sw_kernel(const __grid_constant__ SwArgs a, const __grid_constant__ SwMaps 
                     ++piece;
                 }
                 mma_commit(bar(C::B_ODONE));
+                if (i < 12) FR_STAMP(8 + 4 * i + 3);     // PV_i issued
             };
             // S_{i+1} before PV_i: no cycle, since S_{i+1}'s stages precede V_i's
             // in the ring order. S_i completing also means PV_{i-2} is complete
@@ -486,7 +514,9 @@ attn_sw_kernel(const __grid_constant__ SwArgs a, const __grid_constant__ SwMaps 
                     make_uint4(0u, 0u, 0u, 0u);
             }
             softmax_bar_sync();
+            if (tid == 0) FR_STAMP(5);
             wait(bar(C::B_QF32), 0);
+            if (tid == 0) FR_STAMP(6);           // the f32 Q rows have landed
             const float* q32 = reinterpret_cast<const float*>(sm + C::P_OFF);   // [M][HD]
             const float q_scale = stb.q_scale;
             const int groups = (a.n_head + 3) / 4;         // four heads per item, one cos/sin
@@ -510,6 +540,7 @@ attn_sw_kernel(const __grid_constant__ SwArgs a, const __grid_constant__ SwMaps 
                                                (d1 & 7) * 2) = __float2half_rn(y1);
                 }
             }
+            if (tid == 0) FR_STAMP(7);               // rows roped
             softmax_bar_sync();                  // every f32 row read: the P buffers are free again
         }
         // P^T columns [2NQ, N2) stay zero (the MMA's N is at least 64)
@@ -545,6 +576,7 @@ attn_sw_kernel(const __grid_constant__ SwArgs a, const __grid_constant__ SwMaps 
         }
         for (int i = 0; i < n_my; ++i) {
             wait(bar(C::B_SFULL + (i & 1)), (i >> 1) & 1);
+            if (tid == 0 && i < 12) FR_STAMP(8 + 4 * i);         // softmax of tile i starts
             tc_fence_after();
             float x[RH];
             tmem_ld_cols<RH>(tbase + lane_base + C::TM_S + (i & 1) * NQ + r0, x);
@@ -652,12 +684,14 @@ attn_sw_kernel(const __grid_constant__ SwArgs a, const __grid_constant__ SwMaps 
             }
             fence_proxy_async_cta();            // the tile is read by the tensor cores
             tc_fence_before();
+            if (tid == 0 && i < 12) FR_STAMP(8 + 4 * i + 1);     // P_i written
             mbar_arrive(bar(C::B_PFULL + (i & 1)));
         }
         // every MMA is complete: the issuer commits this barrier once, after the
         // last PV (waiting on ODONE by parity could pass while PV_{n-2} is still
         // running, the barrier then being two phases behind)
         if (!mbar_wait(bar(C::B_MMADONE), 0, limit)) record_timeout(a.status, 1u);
+        if (tid == 0) FR_STAMP(1);               // every MMA complete
         tc_fence_after();
         // row sums: this thread's partials over the warp's keys, then the four
         // lane quadrants, always in the same order
@@ -666,6 +700,7 @@ attn_sw_kernel(const __grid_constant__ SwArgs a, const __grid_constant__ SwMaps 
         softmax_bar_sync();
         if (tid < NQ) sL[tid] = (sRed[tid] + sRed[NQ + tid]) + (sRed[2 * NQ + tid] + sRed[3 * NQ + tid]);
         softmax_bar_sync();
+        if (tid == 0) FR_STAMP(57);              // row sums reduced
         // ---- epilogue: O = O_hi + O_lo; this thread's lane is head dim k of
         // each half, its rows [r0, r0 + RH)
         const int rows = a.M;
@@ -704,6 +739,7 @@ attn_sw_kernel(const __grid_constant__ SwArgs a, const __grid_constant__ SwMaps 
         if (!single && tid < rows)
             a.part_ml[(int64_t)split * a.rstride + tid] =
                 n_my > 0 ? make_float2(sM[tid], sL[tid]) : make_float2(-INFINITY, 0.f);
+        if (tid == 0) FR_STAMP(58);              // rows stored
     }
 
     // ---- the split merge, inside the launch ------------------------------------
@@ -717,27 +753,29 @@ attn_sw_kernel(const __grid_constant__ SwArgs a, const __grid_constant__ SwMaps 
     if (a.splits > 1) {
         __syncthreads();                         // this CTA's state is stored
         if (tid == 0) {
+            // arrive with a release add (this CTA's state is visible before
+            // the count moves), then watch the count itself; the last CTA to
+            // leave returns both words to zero for the next call (the next
+            // call's CTAs arrive only after this grid is complete)
             unsigned* count = a.barrier;
-            unsigned* gen_w = a.barrier + 1;
-            const unsigned gen = ld_acquire_u32(gen_w);    // it cannot move before this CTA arrives
-            __threadfence();
-            if (atomicAdd(count, 1u) == (unsigned)a.splits - 1u) {
-                *count = 0u;                     // ready for the next call
-                __threadfence();
-                atomicAdd(gen_w, 1u);            // release every CTA
-            } else {
-                const uint64_t t_start = global_ns();
-                while (ld_acquire_u32(gen_w) == gen) {
-                    if (global_ns() - t_start > limit) {
-                        record_timeout(a.status, 4u);
-                        break;
-                    }
-                    __nanosleep(32);
+            unsigned* departed = a.barrier + 1;
+            FR_STAMP(59);
+            red_release_add_u32(count, 1u);
+            const uint64_t t_start = global_ns();
+            while (ld_acquire_u32(count) < (unsigned)a.splits) {
+                if (global_ns() - t_start > limit) {
+                    record_timeout(a.status, 4u);
+                    break;
                 }
+                __nanosleep(20);
             }
-            __threadfence();
+            if (atomicAdd(departed, 1u) == (unsigned)a.splits - 1u) {
+                *count = 0u;
+                *departed = 0u;
+            }
         }
         __syncthreads();
+        if (tid == 0) FR_STAMP(56);              // every split's state stored
         constexpr int kWarpMerge = 16;           // up to this many splits, one warp merges a unit alone
         if (warp < kSmaxWarps && a.splits <= kWarpMerge) {
             constexpr int NCH = HD / 32;
@@ -831,6 +869,7 @@ attn_sw_kernel(const __grid_constant__ SwArgs a, const __grid_constant__ SwMaps 
     // ---- teardown ----------------------------------------------------------------
     tc_fence_before();
     __syncthreads();
+    if (tid == 0) FR_STAMP(2);                   // done
     if (warp == kMmaWarp) {
         __syncwarp();
         tc_fence_after();

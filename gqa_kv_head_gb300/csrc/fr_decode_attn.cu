@@ -37,7 +37,7 @@ constexpr int kThreads = kWarps * 32;
 constexpr int kMaxSplits = 32;
 constexpr size_t kWsHeader = 1024;     // [0,4): status word; [256, 256+4*32): tickets
 constexpr size_t kWsTickets = 256;
-constexpr size_t kWsSwBarrier = 512;   // [512, 520): the keys-on-M kernel's grid barrier (count, generation)
+constexpr size_t kWsSwBarrier = 512;   // [512, 520): the keys-on-M kernel's grid barrier (arrivals, departures)
 constexpr float kLog2e = 1.4426950408889634f;
 
 template <int HD>
