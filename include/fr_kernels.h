@@ -295,9 +295,11 @@ fr_status fr_decode_attn_plan(int n_tok, int n_head, int hd, int n_kv, int fused
  * Same arguments and result as fr_decode_attn, minus the workspace. The split
  * state lives in a 9 MiB scratch array inside the library, present on every GPU
  * that loads the library until the process exits. Within it the library picks
- * only plans that fit; shapes whose smallest plan (split states merged inside
- * the attention launch) needs more than 9 MiB, in practice hd = 256 with
- * n_tok*n_head > 256, return FR_ERR_WORKSPACE. No device memory is allocated.
+ * only plans that fit; shapes whose smallest accepted workspace exceeds 9 MiB
+ * return FR_ERR_WORKSPACE. With M = n_tok*n_head those are: hd 64 with
+ * M >= 24065; hd 128 with M >= 12161; hd 256 with 257 <= M <= 512 or
+ * M >= 6047 (the f16 Q slot plus one partial state per row of the 128-row
+ * kernel's in-launch plan). No device memory is allocated.
  * The first call on each device looks up the array's device address
  * (cudaGetSymbolAddress); make that first call before any stream capture. Each
  * call clears the array's arrival tickets on `stream` before launching; its

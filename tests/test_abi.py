@@ -201,3 +201,23 @@ def test_binding_has_no_cpu_path():
     with pytest.raises(ValueError):
         fr.decode_attn(torch.zeros(4, 64, dtype=torch.float16), torch.zeros(4, 64, dtype=torch.float16),
                        1, 1, q16=torch.zeros(1, 64, dtype=torch.float16))
+
+
+def test_noalloc_size_limit_matches_the_documented_thresholds(lib):
+    """The smallest workspace fr_decode_attn accepts, against the 9 MiB scratch
+    of fr_decode_attn_noalloc: the thresholds include/fr_kernels.h states
+    (host-side sizing only; without a GPU a fitting call stops at the device
+    query, FR_ERR_CUDA, and one that does not fit at FR_ERR_WORKSPACE)."""
+    from gqa_kv_head_gb300._abi import FrAttnPlan
+    plan = FrAttnPlan()
+
+    def fits(n_tok, n_head, hd, n_kv=4096):
+        st = lib.fr_decode_attn_plan(n_tok, n_head, hd, n_kv, 1, 9 << 20, None, ctypes.byref(plan))
+        assert st in (0, 3, 4), st
+        return st != 3
+    assert fits(16, 16, 256) and not fits(16, 17, 256)          # M 256 | 272
+    assert not fits(16, 32, 256) and fits(80, 8, 256)           # M 512 | 640
+    assert fits(755, 8, 256) and not fits(756, 8, 256)          # M 6040 | 6048
+    assert fits(1520, 8, 128) and not fits(1521, 8, 128)        # M 12160 | 12168
+    assert fits(3008, 8, 64) and not fits(3009, 8, 64)          # M 24064 | 24072
+    assert fits(1, 8, 256, 65536) and fits(4, 8, 128, 65536)    # keys-on-M plans need only the Q slot
