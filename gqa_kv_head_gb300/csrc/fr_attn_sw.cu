@@ -10,10 +10,12 @@
 // padding; here 128 keys are the MMA's M and the query rows its N (16, 32 or
 // 64), so the tensor work follows the real rows.
 //
-// One CTA = one KV split (one CTA per SM), 320 threads:
-//   warps 0-7  softmax, one thread per (key of the tile, half of the query
-//              rows): warps w and w + 4 share TMEM lane quadrant w (keys
-//              32w..32w+31 of S^T) and take rows [0, NQ/2) and [NQ/2, NQ).
+// One CTA = one KV split (one CTA per SM); W softmax warps (8 for 16 rows,
+// 16 for 32 or 64 rows) and two more:
+//   warps 0..W-1  softmax, one thread per (key of the tile, W/4-th of the
+//              query rows): warps w, w + 4, ... share TMEM lane quadrant w % 4
+//              (keys 32(w%4)..+31 of S^T), each owning a slice of at most 16
+//              rows.
 //              kq_scale and the mask; the per-row reference maxima are only
 //              recomputed when some score exceeds its row's reference by more
 //              than 2^8 (one barrier-OR vote per tile; the row maxima then come
@@ -23,11 +25,11 @@
 //              per key) as the B operand of the PV MMA; partial row sums per
 //              thread. After the loop the same threads own the TMEM lanes of
 //              O^T (lane = head dim) for the epilogue, where O = O_hi + O_lo.
-//   warp 8     TMA producer: one ring of 32 KiB stages (128 keys x 128 dims of
+//   warp W     TMA producer: one ring of 32 KiB stages (128 keys x 128 dims of
 //              K or of V, two 64-dim boxes) filled in exactly the order the
 //              MMAs consume them, a ring of mask tiles, and in the fused call
 //              the f32 Q rows (one bulk copy per token) for the in-kernel RoPE.
-//   warp 9     MMA issuer: S^T_j = K_j Q^T (A = K stage, K-major; B = the Q
+//   warp W+1   MMA issuer: S^T_j = K_j Q^T (A = K stage, K-major; B = the Q
 //              rows), O^T += V_j^T [P_hi; P_lo]^T (A = V stage and B = P^T, both
 //              read MN-major; the P_lo product accumulates in its own columns).
 //              S_{j+1} is issued before PV_j, so the softmax of tile j+1
@@ -73,11 +75,6 @@ using namespace sm100;
 #endif
 
 constexpr int kKeys = 128;               // keys per KV tile = the MMA's M
-constexpr int kSmaxWarps = 8;            // two per TMEM lane quadrant
-constexpr int kSmaxThreads = kSmaxWarps * 32;
-constexpr int kProdWarp = 8;
-constexpr int kMmaWarp = 9;
-constexpr int kThreads = (kSmaxWarps + 2) * 32;
 constexpr float kTau = 8.0f;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr int kBox = 16384;              // 128 rows x 128 bytes (64 f16), 128-byte swizzle
@@ -89,7 +86,13 @@ struct Cfg {
     static_assert(HD == 128 || HD == 256, "head dims");
     static_assert(NQ == 16 || NQ == 32 || NQ == 64, "query rows");
     static constexpr int HALVES = HD / 128;          // K (and V) stages per tile
-    static constexpr int RH = NQ / 2;                // rows per softmax thread
+    // softmax warps: 8 (two per TMEM lane quadrant) for 16 rows, 16 (four per
+    // quadrant) for 32 or 64 rows, so that a thread owns at most 16 rows
+    static constexpr int SMW = NQ >= 32 ? 16 : 8;
+    static constexpr int SMT = SMW * 32;             // softmax threads
+    static constexpr int PROD_WARP = SMW, MMA_WARP = SMW + 1;
+    static constexpr int THREADS = (SMW + 2) * 32;
+    static constexpr int RH = NQ / (SMW / 4);        // rows per softmax thread
     static constexpr int N2 = 2 * NQ < 64 ? 64 : 2 * NQ;   // PV MMA N: [P_hi | P_lo | zeros]
     static constexpr int Q_BOX = NQ * 128;           // 64 dims of the NQ rows (K-major)
     static constexpr int Q_BYTES = (HD / 64) * Q_BOX;
@@ -123,6 +126,7 @@ struct Cfg {
     static constexpr int AUX_POS = AUX_FLAG + 16;    // [kMaskWin] token positions (fused call)
     static constexpr int AUX_TB = (AUX_POS + kMaskWin * 4 + 15) / 16 * 16;
     static_assert(AUX_TB + (int)sizeof(RopeTable) <= AUX, "aux");
+    static_assert(RH % 8 == 0, "P rows per thread: whole 16-byte chunks");
     static constexpr int B_FULL = 0, B_EMPTY = R, B_MFULL = 2 * R, B_MEMPTY = 2 * R + MS,
                          B_SFULL = 2 * (R + MS), B_PFULL = B_SFULL + 2, B_ODONE = B_SFULL + 4,
                          B_QFULL = B_SFULL + 5, B_MMADONE = B_SFULL + 6, B_PROBE = B_SFULL + 7,
@@ -190,15 +194,17 @@ __device__ __forceinline__ unsigned ld_acquire_u32(const unsigned* p) {
     return v;
 }
 
-// Barrier over the softmax warps (named barrier 1).
+// Barrier over the N softmax threads (named barrier 1).
+template <int N>
 __device__ __forceinline__ void softmax_bar_sync() {
-    asm volatile("bar.sync 1, %0;" :: "n"(kSmaxThreads) : "memory");
+    asm volatile("bar.sync 1, %0;" :: "n"(N) : "memory");
 }
 // The same barrier, returning whether any softmax thread passed a true vote.
+template <int N>
 __device__ __forceinline__ bool softmax_bar_any(bool vote) {
     uint32_t r;
     asm volatile("{ .reg .pred p, q; setp.ne.u32 q, %1, 0; bar.red.or.pred p, 1, %2, q; selp.u32 %0, 1, 0, p; }"
-                 : "=r"(r) : "r"((uint32_t)vote), "n"(kSmaxThreads) : "memory");
+                 : "=r"(r) : "r"((uint32_t)vote), "n"(N) : "memory");
     return r != 0;
 }
 
@@ -226,11 +232,13 @@ __device__ __forceinline__ void tmem_st_cols(uint32_t taddr, const float* x) {
 }
 
 template <int HD, int NQ>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(Cfg<HD, NQ>::THREADS, 1)
 attn_sw_kernel(const __grid_constant__ SwArgs a, const __grid_constant__ SwMaps mp,
                const __grid_constant__ RopeTable tb) {
     using C = Cfg<HD, NQ>;
     constexpr int RH = C::RH;
+    constexpr int kSmaxWarps = C::SMW, kSmaxThreads = C::SMT;
+    constexpr int kProdWarp = C::PROD_WARP, kMmaWarp = C::MMA_WARP;
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     unsigned char* sm = reinterpret_cast<unsigned char*>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     uint64_t* bars = reinterpret_cast<uint64_t*>(sm + C::BAR_OFF);
@@ -292,6 +300,14 @@ attn_sw_kernel(const __grid_constant__ SwArgs a, const __grid_constant__ SwMaps 
     tc_fence_after();
     const uint32_t tbase = *sTmemBase;
     if (tid == 0) FR_STAMP(0);                   // set-up done
+#ifdef FR_TRACE
+    if (tid == 0) {
+        unsigned smid;
+        asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
+        reinterpret_cast<unsigned long long*>(reinterpret_cast<unsigned char*>(a.status) + FR_TRACE_OFFSET)
+            [blockIdx.x * 64 + 63] = smid;       // the SM this CTA runs on
+    }
+#endif
     // a dependent grid (the merge kernel, or the next call) may be scheduled
     // now; it waits for this grid's completion before reading what this grid
     // writes. Only when this grid is one wave.
@@ -513,7 +529,7 @@ attn_sw_kernel(const __grid_constant__ SwArgs a, const __grid_constant__ SwMaps 
                 *reinterpret_cast<uint4*>(sQ + (ch >> 3) * C::Q_BOX + r * 128 + ((ch & 7) << 4)) =
                     make_uint4(0u, 0u, 0u, 0u);
             }
-            softmax_bar_sync();
+            softmax_bar_sync<kSmaxThreads>();
             if (tid == 0) FR_STAMP(5);
             wait(bar(C::B_QF32), 0);
             if (tid == 0) FR_STAMP(6);           // the f32 Q rows have landed
@@ -541,7 +557,7 @@ attn_sw_kernel(const __grid_constant__ SwArgs a, const __grid_constant__ SwMaps 
                 }
             }
             if (tid == 0) FR_STAMP(7);               // rows roped
-            softmax_bar_sync();                  // every f32 row read: the P buffers are free again
+            softmax_bar_sync<kSmaxThreads>();                  // every f32 row read: the P buffers are free again
         }
         // P^T columns [2NQ, N2) stay zero (the MMA's N is at least 64)
         if constexpr (2 * NQ < C::N2) {
@@ -608,13 +624,13 @@ attn_sw_kernel(const __grid_constant__ SwArgs a, const __grid_constant__ SwMaps 
             // reference by more than 2^8: then the row maxima of this tile are
             // reduced (warp shuffles, then the four lane quadrants), and every
             // row whose maximum exceeded its reference takes it
-            if (softmax_bar_any(over)) {
+            if (softmax_bar_any<kSmaxThreads>(over)) {
                 float v[RH];
 #pragma unroll
                 for (int u = 0; u < RH; ++u) v[u] = x[u];
                 ReduceScatter<16, RH, RH, true>::run(v, lane);
                 if (writer) sRed[qd * NQ + r0 + rb] = v[0];
-                softmax_bar_sync();
+                softmax_bar_sync<kSmaxThreads>();
                 if (tid < NQ) {
                     const float tm = fmaxf(fmaxf(sRed[tid], sRed[NQ + tid]), fmaxf(sRed[2 * NQ + tid], sRed[3 * NQ + tid]));
                     const float m_old = sM[tid];
@@ -625,7 +641,7 @@ attn_sw_kernel(const __grid_constant__ SwArgs a, const __grid_constant__ SwMaps 
                     sM[tid] = m_new;
                     if (grow) sFlag[0] = 1;
                 }
-                softmax_bar_sync();
+                softmax_bar_sync<kSmaxThreads>();
                 const bool grew = sFlag[0] != 0;
 #pragma unroll
                 for (int u = 0; u < RH; ++u) mref[u] = sM[r0 + u];
@@ -655,7 +671,7 @@ attn_sw_kernel(const __grid_constant__ SwArgs a, const __grid_constant__ SwMaps 
                         tmem_wait_st();
                     }
                 }
-                softmax_bar_sync();                      // everyone has read sFlag and sM
+                softmax_bar_sync<kSmaxThreads>();                      // everyone has read sFlag and sM
                 if (tid == 0) sFlag[0] = 0;
             }
             // P = 2^(x - m) as f16 P_hi and P_lo: row k of the MN-major B operand
@@ -697,9 +713,9 @@ attn_sw_kernel(const __grid_constant__ SwArgs a, const __grid_constant__ SwMaps 
         // lane quadrants, always in the same order
         ReduceScatter<16, RH, RH, false>::run(l_part, lane);
         if (writer) sRed[qd * NQ + r0 + rb] = l_part[0];
-        softmax_bar_sync();
+        softmax_bar_sync<kSmaxThreads>();
         if (tid < NQ) sL[tid] = (sRed[tid] + sRed[NQ + tid]) + (sRed[2 * NQ + tid] + sRed[3 * NQ + tid]);
-        softmax_bar_sync();
+        softmax_bar_sync<kSmaxThreads>();
         if (tid == 0) FR_STAMP(57);              // row sums reduced
         // ---- epilogue: O = O_hi + O_lo; this thread's lane is head dim k of
         // each half, its rows [r0, r0 + RH)
@@ -745,11 +761,9 @@ attn_sw_kernel(const __grid_constant__ SwArgs a, const __grid_constant__ SwMaps 
     // ---- the split merge, inside the launch ------------------------------------
     // Every CTA is resident (cooperative launch, one CTA per SM), so a bounded
     // grid barrier is safe: once every split's state is stored, CTA b merges
-    // the units (row, 32 columns) b, b + splits, ... Each softmax warp loads
-    // its share of the splits' states for a unit in one round (all loads in
-    // flight), the warps combine through shared memory in a fixed order; with
-    // few splits every warp merges whole units on its own. A wait that gives
-    // up sets the status word and the CTA carries on.
+    // the output in units of (row, 32 columns), spread over every softmax warp
+    // of the grid (below). A wait that gives up sets the status word and the
+    // CTA carries on.
     if (a.splits > 1) {
         __syncthreads();                         // this CTA's state is stored
         if (tid == 0) {
@@ -776,92 +790,86 @@ attn_sw_kernel(const __grid_constant__ SwArgs a, const __grid_constant__ SwMaps 
         }
         __syncthreads();
         if (tid == 0) FR_STAMP(56);              // every split's state stored
-        constexpr int kWarpMerge = 16;           // up to this many splits, one warp merges a unit alone
-        if (warp < kSmaxWarps && a.splits <= kWarpMerge) {
+        if (warp < kSmaxWarps) {
+            // a group of G warps per unit, G the largest power of two with one
+            // group per unit over the whole grid (at most every softmax warp of
+            // a CTA); warp j of a group folds splits j, j + G, ... in chunks
+            // with every load of a chunk in flight (online: the running
+            // maximum rescales what is folded so far), and the group combines
+            // its warps through shared memory, always in the same order
             constexpr int NCH = HD / 32;
+            // one chunk covers a warp's share whenever G = every softmax warp
+            constexpr int CHUNK = (tc::kMaxMergeSplits + kSmaxWarps - 1) / kSmaxWarps;
             const int units = a.M * NCH;
             const int S = a.splits;
-            for (int u = split * kSmaxWarps + warp; u < units; u += S * kSmaxWarps) {
-                const int r = u / NCH, c0 = (u - r * NCH) * 32;
-                float2 ml[kWarpMerge];
-                float ov[kWarpMerge];
+            const int per = (S * kSmaxWarps) / units;          // warps of the grid per unit
+            int G = 1;
+            while (G * 2 <= kSmaxWarps && G * 2 <= per) G *= 2;
+            const int groups = kSmaxWarps / G;                  // per CTA
+            const int gi = warp / G, j = warp - gi * G;
+            float* sAcc = reinterpret_cast<float*>(sm + C::RING_OFF);     // [warps][32] (the ring is idle)
+            float* sMw = sAcc + kSmaxWarps * 32;                        // [warps]
+            float* sLw = sMw + kSmaxWarps;                              // [warps]
+            const int rounds = (units + S * groups - 1) / (S * groups); // the same for every warp
+            for (int rd = 0; rd < rounds; ++rd) {
+                const int u = (rd * S + split) * groups + gi;
+                const bool live = u < units;
+                const int r = live ? u / NCH : 0, c0 = live ? (u - (u / NCH) * NCH) * 32 : 0;
+                float mx = -INFINITY, acc = 0.f, L = 0.f;
+                for (int s0 = j; live && s0 < S; s0 += CHUNK * G) {
+                    float2 ml[CHUNK];
+                    float ov[CHUNK];
 #pragma unroll
-                for (int j = 0; j < kWarpMerge; ++j) {
-                    if (j < S) {
-                        const int64_t row = (int64_t)j * a.rstride + r;
-                        ml[j] = __ldcg(a.part_ml + row);
-                        ov[j] = __ldcg(a.part_o + row * HD + c0 + lane);
-                    } else {
-                        ml[j] = make_float2(-INFINITY, 0.f);
-                        ov[j] = 0.f;
+                    for (int t = 0; t < CHUNK; ++t) {
+                        const int s2 = s0 + t * G;
+                        if (s2 < S) {
+                            const int64_t row = (int64_t)s2 * a.rstride + r;
+                            ml[t] = __ldcg(a.part_ml + row);
+                            ov[t] = __ldcg(a.part_o + row * HD + c0 + lane);
+                        } else {
+                            ml[t] = make_float2(-INFINITY, 0.f);
+                            ov[t] = 0.f;
+                        }
+                    }
+                    float cm = mx;
+#pragma unroll
+                    for (int t = 0; t < CHUNK; ++t) cm = fmaxf(cm, ml[t].x);
+                    if (cm != -INFINITY) {
+                        const float sc = mx == -INFINITY ? 0.f : ex2(mx - cm);
+                        acc *= sc;
+                        L *= sc;
+#pragma unroll
+                        for (int t = 0; t < CHUNK; ++t) {
+                            const float w = ml[t].x == -INFINITY ? 0.f : ex2(ml[t].x - cm);
+                            L = fmaf(w, ml[t].y, L);
+                            acc = fmaf(w, ov[t], acc);
+                        }
+                        mx = cm;
                     }
                 }
-                float mx = -INFINITY;
-#pragma unroll
-                for (int j = 0; j < kWarpMerge; ++j) mx = fmaxf(mx, ml[j].x);
-                const float ref = mx == -INFINITY ? 0.f : mx;
-                float acc = 0.f, L = 0.f;
-#pragma unroll
-                for (int j = 0; j < kWarpMerge; ++j) {          // split order: deterministic
-                    const float w = ml[j].x == -INFINITY ? 0.f : ex2(ml[j].x - ref);
-                    L = fmaf(w, ml[j].y, L);
-                    acc = fmaf(w, ov[j], acc);
-                }
-                a.out[(int64_t)r * HD + c0 + lane] = L > 0.f ? acc / L : 0.f;
-            }
-        } else if (warp < kSmaxWarps) {
-            constexpr int NCH = HD / 32;
-            constexpr int PW = (tc::kMaxMergeSplits + kSmaxWarps - 1) / kSmaxWarps;   // splits per warp
-            float* sAcc = reinterpret_cast<float*>(sm + C::RING_OFF);          // [8][32] (the ring is idle)
-            float* sMw = sAcc + kSmaxWarps * 32;                             // [8] warp maxima
-            float* sLw = sMw + kSmaxWarps;                                   // [8] weighted sums
-            const int units = a.M * NCH;
-            const int S = a.splits;
-            for (int u = split; u < units; u += S) {
-                const int r = u / NCH, c0 = (u - r * NCH) * 32;
-                float2 ml[PW];
-                float ov[PW];
-#pragma unroll
-                for (int j = 0; j < PW; ++j) {
-                    const int s2 = warp + j * kSmaxWarps;
-                    if (s2 < S) {
-                        const int64_t row = (int64_t)s2 * a.rstride + r;
-                        ml[j] = __ldcg(a.part_ml + row);
-                        ov[j] = __ldcg(a.part_o + row * HD + c0 + lane);
-                    } else {
-                        ml[j] = make_float2(-INFINITY, 0.f);
-                        ov[j] = 0.f;
+                if (G == 1) {
+                    if (live) a.out[(int64_t)r * HD + c0 + lane] = L > 0.f ? acc / L : 0.f;
+                } else {
+                    sAcc[warp * 32 + lane] = acc;
+                    if (lane == 0) {
+                        sMw[warp] = mx;
+                        sLw[warp] = L;
                     }
-                }
-                float mw = -INFINITY;
-#pragma unroll
-                for (int j = 0; j < PW; ++j) mw = fmaxf(mw, ml[j].x);
-                if (lane == 0) sMw[warp] = mw;
-                softmax_bar_sync();
-                float mx = -INFINITY;
-#pragma unroll
-                for (int w = 0; w < kSmaxWarps; ++w) mx = fmaxf(mx, sMw[w]);
-                const float ref = mx == -INFINITY ? 0.f : mx;
-                float acc = 0.f, L = 0.f;
-#pragma unroll
-                for (int j = 0; j < PW; ++j) {
-                    const float w = ml[j].x == -INFINITY ? 0.f : ex2(ml[j].x - ref);
-                    L = fmaf(w, ml[j].y, L);
-                    acc = fmaf(w, ov[j], acc);
-                }
-                sAcc[warp * 32 + lane] = acc;
-                if (lane == 0) sLw[warp] = L;
-                softmax_bar_sync();
-                if (warp == 0) {
-                    float sum = 0.f, Lt = 0.f;
-#pragma unroll
-                    for (int w = 0; w < kSmaxWarps; ++w) {              // always the same order
-                        sum += sAcc[w * 32 + lane];
-                        Lt += sLw[w];
+                    softmax_bar_sync<kSmaxThreads>();
+                    if (j == 0 && live) {
+                        float gm = -INFINITY;
+                        for (int w = 0; w < G; ++w) gm = fmaxf(gm, sMw[warp + w]);
+                        float sum = 0.f, Lt = 0.f;
+                        for (int w = 0; w < G; ++w) {                  // always the same order
+                            const float mw = sMw[warp + w];
+                            const float sc = mw == -INFINITY ? 0.f : ex2(mw - gm);
+                            sum = fmaf(sc, sAcc[(warp + w) * 32 + lane], sum);
+                            Lt = fmaf(sc, sLw[warp + w], Lt);
+                        }
+                        a.out[(int64_t)r * HD + c0 + lane] = Lt > 0.f ? sum / Lt : 0.f;
                     }
-                    a.out[(int64_t)r * HD + c0 + lane] = Lt > 0.f ? sum / Lt : 0.f;
+                    softmax_bar_sync<kSmaxThreads>();
                 }
-                softmax_bar_sync();
             }
         }
     }
@@ -907,7 +915,7 @@ static fr_status launch(const SwLaunch& L, cudaStream_t stream) {
     cudaLaunchConfig_t cfg;
     memset(&cfg, 0, sizeof(cfg));
     cfg.gridDim = dim3(a.splits, 1, 1);
-    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.blockDim = dim3(Cfg<HD, NQ>::THREADS, 1, 1);
     cfg.dynamicSmemBytes = Cfg<HD, NQ>::SMEM;
     cfg.stream = stream;
     // several splits merge behind a grid barrier: every CTA must be resident

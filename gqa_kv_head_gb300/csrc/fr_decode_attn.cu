@@ -419,9 +419,9 @@ static bool sw_shape_ok(int n_tok, int n_head, int hd) {
 }
 // The library's choice (measured on GB300, graph replay of fused calls): the
 // keys-on-M kernel wins by 10-25 % at up to 32 query rows when there are at
-// least 1024 keys and 128 per row; at 64 rows its softmax (32 rows per thread)
-// is slower than the 128-row kernel's, and with fewer keys its few splits
-// leave each merging warp many (row, 32-column) units.
+// least 1024 keys and 256 per row; at 64 rows its softmax is slower than the
+// 128-row kernel's, and with fewer keys per row its short loop does not pay for
+// its in-launch merge.
 static constexpr int kSwAutoRows = 32;
 static constexpr int kSwAutoKeys = 1024;
 static bool use_sw(int n_tok, int n_head, int hd, int n_kv, const fr_attn_opts& o) {
@@ -429,7 +429,7 @@ static bool use_sw(int n_tok, int n_head, int hd, int n_kv, const fr_attn_opts& 
     if (o.layout == 2) return true;
     if (o.layout == 1 || o.force_cluster != 0 || o.merge_mode == 1) return false;
     const int M = n_tok * n_head;
-    return M <= kSwAutoRows && n_kv >= kSwAutoKeys && n_kv >= 128 * M;
+    return M <= kSwAutoRows && n_kv >= kSwAutoKeys && n_kv >= 256 * M;
 }
 
 // Smallest workspace the plan a call with these options takes accepts: the

@@ -59,6 +59,8 @@ def main(argv):
         st.synchronize()
         S = plan["splits"]
         tr = ws[TRACE_OFFSET:TRACE_OFFSET + S * SLOTS * 8].view(torch.int64).view(S, SLOTS).cpu().numpy()
+        smid = tr[:, 63].copy()
+        tr[:, 63] = tr[:, 0]
         rel = (tr - tr[:, 0].min()) / 1000.0
         med = lambda c: float(np.median(rel[:, c]))
         n_tiles = (w.n_kv // S + 127) // 128
@@ -69,6 +71,10 @@ def main(argv):
               f"{med(59):.2f} (last {rel[:, 59].max():.2f})")
         print(f"every MMA done {rel[:, 1].min():.2f} .. {rel[:, 1].max():.2f}; split states stored "
               f"{rel[:, 56].min():.2f} .. {rel[:, 56].max():.2f}; end {rel[:, 2].min():.2f} .. {rel[:, 2].max():.2f}")
+        order = np.argsort(rel[:, 1])
+        print("last MMA done, slowest 12 CTAs (cta/sm: us): " + ", ".join(
+            f"{int(b)}/{int(smid[b])}: {rel[b, 1]:.2f}" for b in order[::-1][:12]))
+        print("fastest 6: " + ", ".join(f"{int(b)}/{int(smid[b])}: {rel[b, 1]:.2f}" for b in order[:6]))
         c = int(np.argsort(rel[:, 2])[S // 2])
         tiles = "  ".join(
             f"t{i}: S {rel[c, 8 + 4 * i + 2]:.2f} softmax {rel[c, 8 + 4 * i]:.2f}-{rel[c, 8 + 4 * i + 1]:.2f} "

@@ -252,7 +252,7 @@ typedef struct fr_attn_opts {
                               are the MMA's M); 2 = 128-key tiles as the MMA's M and the
                               query rows as its N (M <= 64 rows, hd 128 or 256, n_tok <= 16:
                               FR_ERR_UNSUPPORTED otherwise). The library's choice is 2 for
-                              M <= 32 rows and n_kv >= max(1024, 128 M) (where it measures
+                              M <= 32 rows and n_kv >= max(1024, 256 M) (where it measures
                               faster), unless force_cluster or merge_mode 1 is given. */
 } fr_attn_opts;
 

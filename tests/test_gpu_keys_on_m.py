@@ -27,7 +27,7 @@ def _plan(w, **kw):
     return fr.decode_attn_plan(w.n_tok, w.n_head, w.hd, w.n_kv, layout=2, **kw)
 
 
-KOM = dict(layout=2)      # the library picks this layout itself for M <= 32 rows and n_kv >= max(1024, 128 M)
+KOM = dict(layout=2)      # the library picks this layout itself for M <= 32 rows and n_kv >= max(1024, 256 M)
 
 
 @pytest.mark.parametrize("hd", [128, 256])
@@ -39,7 +39,7 @@ def test_row_counts(hd, n_tok, n_head):
                  mask_kind="causal", seed=n_tok * 7 + n_head)
     assert _plan(w)["keys_on_m"] == 1
     auto = fr.decode_attn_plan(w.n_tok, w.n_head, w.hd, w.n_kv)["keys_on_m"]
-    assert auto == (1 if w.M <= 32 and w.n_kv >= max(1024, 128 * w.M) else 0)
+    assert auto == (1 if w.M <= 32 and w.n_kv >= max(1024, 256 * w.M) else 0)
     d = to_device(w)
     out = _rows(run_fused(w, d, **KOM))
     ref = oracle_out(w)
