@@ -40,7 +40,7 @@ class FrAttnOpts(ctypes.Structure):
 class FrAttnPlan(ctypes.Structure):
     _fields_ = [("engine", ctypes.c_int), ("row_tiles", ctypes.c_int), ("splits", ctypes.c_int),
                 ("cluster", ctypes.c_int), ("merge_kernel", ctypes.c_int), ("launches", ctypes.c_int),
-                ("keys_on_m", ctypes.c_int)]
+                ("keys_on_m", ctypes.c_int), ("layout", ctypes.c_int)]
 
 
 _P = ctypes.c_void_p

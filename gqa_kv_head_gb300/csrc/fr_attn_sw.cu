@@ -49,30 +49,13 @@
 #include "fr_attn.h"
 #include "fr_common.cuh"
 #include "fr_sm100.cuh"
+#include "fr_split_merge.cuh"
+#include "fr_trace.cuh"
 
 namespace fr {
 namespace sw {
 
 using namespace sm100;
-
-// Timeline instrumentation (compile-time option, off in the library): with
-// FR_TRACE defined, CTA b writes global-timer stamps into 64 slots at
-// workspace + FR_TRACE_OFFSET + 512 b (gqa_kv_head_gb300.trace builds that
-// variant into its own library and prints the timeline).
-#ifdef FR_TRACE
-#ifndef FR_TRACE_OFFSET
-#define FR_TRACE_OFFSET (32u << 20)
-#endif
-#define FR_STAMP(i)                                                                                         \
-    do {                                                                                                    \
-        reinterpret_cast<unsigned long long*>(reinterpret_cast<unsigned char*>(a.status) + FR_TRACE_OFFSET)  \
-            [blockIdx.x * 64 + (i)] = global_ns();                                                          \
-    } while (0)
-#else
-#define FR_STAMP(i) \
-    do {            \
-    } while (0)
-#endif
 
 constexpr int kKeys = 128;               // keys per KV tile = the MMA's M
 constexpr float kTau = 8.0f;
@@ -185,15 +168,6 @@ __device__ __forceinline__ int rs_row(int lane) {
 }
 
 __device__ __forceinline__ void record_timeout(unsigned* status, unsigned bit) { atomicOr(status, bit); }
-__device__ __forceinline__ void red_release_add_u32(unsigned* p, unsigned v) {
-    asm volatile("red.release.gpu.global.add.u32 [%0], %1;" :: "l"(p), "r"(v) : "memory");
-}
-__device__ __forceinline__ unsigned ld_acquire_u32(const unsigned* p) {
-    unsigned v;
-    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-    return v;
-}
-
 // Barrier over the N softmax threads (named barrier 1).
 template <int N>
 __device__ __forceinline__ void softmax_bar_sync() {
@@ -300,14 +274,7 @@ attn_sw_kernel(const __grid_constant__ SwArgs a, const __grid_constant__ SwMaps 
     tc_fence_after();
     const uint32_t tbase = *sTmemBase;
     if (tid == 0) FR_STAMP(0);                   // set-up done
-#ifdef FR_TRACE
-    if (tid == 0) {
-        unsigned smid;
-        asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
-        reinterpret_cast<unsigned long long*>(reinterpret_cast<unsigned char*>(a.status) + FR_TRACE_OFFSET)
-            [blockIdx.x * 64 + 63] = smid;       // the SM this CTA runs on
-    }
-#endif
+    if (tid == 0) FR_STAMP_SMID();
     // a dependent grid (the merge kernel, or the next call) may be scheduled
     // now; it waits for this grid's completion before reading what this grid
     // writes. Only when this grid is one wave.
@@ -504,21 +471,7 @@ attn_sw_kernel(const __grid_constant__ SwArgs a, const __grid_constant__ SwMaps 
             // cos/sin per (token, pair), shared by the token's heads; rows >= M
             // are zero
             RopeTable& stb = *reinterpret_cast<RopeTable*>(sm + C::AUX_OFF + C::AUX_TB);
-            for (int c = tid; c < HD / 2; c += kSmaxThreads) {
-                stb.turns[c] = tb.turns[c];
-                stb.mix[c] = tb.mix[c];
-                stb.ff[c] = tb.ff[c];
-            }
-            if (tid == 0) {
-                stb.mscale = tb.mscale;
-                stb.q_scale = tb.q_scale;
-                stb.theta_scale = tb.theta_scale;
-                stb.freq_scale = tb.freq_scale;
-                stb.half = tb.half;
-                stb.n_dims = tb.n_dims;
-                stb.mode = tb.mode;
-                stb.yarn = tb.yarn;
-            }
+            copy_rope_table(stb, tb, tid, kSmaxThreads);
             asm volatile("griddepcontrol.wait;" ::: "memory");     // pos may come from the grid before
             // the positions now, before the K/V stream starts (the RoPE needs them)
             int* sPos = reinterpret_cast<int*>(sm + C::AUX_OFF + C::AUX_POS);
@@ -533,29 +486,8 @@ attn_sw_kernel(const __grid_constant__ SwArgs a, const __grid_constant__ SwMaps 
             if (tid == 0) FR_STAMP(5);
             wait(bar(C::B_QF32), 0);
             if (tid == 0) FR_STAMP(6);           // the f32 Q rows have landed
-            const float* q32 = reinterpret_cast<const float*>(sm + C::P_OFF);   // [M][HD]
-            const float q_scale = stb.q_scale;
-            const int groups = (a.n_head + 3) / 4;         // four heads per item, one cos/sin
-            for (int it = tid; it < a.n_tok * groups * (HD / 2); it += kSmaxThreads) {
-                const int c = it % (HD / 2), tg = it / (HD / 2);
-                const int t = tg / groups, h0 = (tg - t * groups) * 4;
-                int d0, d1;
-                rope_slot_dims(c, stb, d0, d1);
-                const bool rot = c < stb.half;
-                float cs = 0.f, sn = 0.f;
-                if (rot) rope_cs_tab(sPos[t], c, stb, cs, sn);
-                for (int h = h0; h < min(h0 + 4, a.n_head); ++h) {
-                    const int r = t * a.n_head + h;
-                    const float x0 = q32[r * HD + d0], x1 = q32[r * HD + d1];
-                    const float y0 = rot ? rope_lo(x0, x1, cs, sn, q_scale) : __fmul_rn(x0, q_scale);
-                    const float y1 = rot ? rope_hi(x0, x1, cs, sn, q_scale) : __fmul_rn(x1, q_scale);
-                    unsigned char* row = sQ + r * 128;
-                    *reinterpret_cast<__half*>(row + (d0 >> 6) * C::Q_BOX + ((((d0 & 63) >> 3) ^ (r & 7)) << 4) +
-                                               (d0 & 7) * 2) = __float2half_rn(y0);
-                    *reinterpret_cast<__half*>(row + (d1 >> 6) * C::Q_BOX + ((((d1 & 63) >> 3) ^ (r & 7)) << 4) +
-                                               (d1 & 7) * 2) = __float2half_rn(y1);
-                }
-            }
+            rope_rows_to_tile<HD>(reinterpret_cast<const float*>(sm + C::P_OFF), sPos, stb, a.n_tok, a.n_head, sQ,
+                                  C::Q_BOX, tid, kSmaxThreads);
             if (tid == 0) FR_STAMP(7);               // rows roped
             softmax_bar_sync<kSmaxThreads>();                  // every f32 row read: the P buffers are free again
         }
@@ -767,26 +699,8 @@ attn_sw_kernel(const __grid_constant__ SwArgs a, const __grid_constant__ SwMaps 
     if (a.splits > 1) {
         __syncthreads();                         // this CTA's state is stored
         if (tid == 0) {
-            // arrive with a release add (this CTA's state is visible before
-            // the count moves), then watch the count itself; the last CTA to
-            // leave returns both words to zero for the next call (the next
-            // call's CTAs arrive only after this grid is complete)
-            unsigned* count = a.barrier;
-            unsigned* departed = a.barrier + 1;
             FR_STAMP(59);
-            red_release_add_u32(count, 1u);
-            const uint64_t t_start = global_ns();
-            while (ld_acquire_u32(count) < (unsigned)a.splits) {
-                if (global_ns() - t_start > limit) {
-                    record_timeout(a.status, 4u);
-                    break;
-                }
-                __nanosleep(20);
-            }
-            if (atomicAdd(departed, 1u) == (unsigned)a.splits - 1u) {
-                *count = 0u;
-                *departed = 0u;
-            }
+            if (!split_merge::grid_barrier(a.barrier, (unsigned)a.splits, limit)) record_timeout(a.status, 4u);
         }
         __syncthreads();
         if (tid == 0) FR_STAMP(56);              // every split's state stored

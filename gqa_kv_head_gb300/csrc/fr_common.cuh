@@ -142,6 +142,59 @@ __device__ __forceinline__ void rope_slot(const float* __restrict__ qrow, int c,
     rope_slot_apply(c, qrow[d0], qrow[d1], pos, tb, y0, y1);
 }
 
+// The f16 Q tile of an attention kernel that ropes its own rows: row
+// r = t*n_head + h (t-major, the order qkv_post emits) from the f32 rows
+// staged in shared memory at q32[r*HD], written K-major in the 128-byte
+// swizzle (64 dims per box of q_box bytes, 128 bytes per row). One work item
+// is (token, slot, group of kQkvHeads heads) with one cos/sin, and every value
+// goes through rope_cs_tab / rope_lo / rope_hi like qkv_post's: the bits equal
+// its f16 rows. Called by threads [0, nthreads) with their index tid.
+template <int HD>
+__device__ __forceinline__ void rope_rows_to_tile(const float* q32, const int* pos, const RopeTable& tb, int n_tok,
+                                                  int n_head, unsigned char* tile, int q_box, int tid, int nthreads) {
+    const int groups = (n_head + kQkvHeads - 1) / kQkvHeads;
+    for (int it = tid; it < n_tok * groups * (HD / 2); it += nthreads) {
+        const int c = it % (HD / 2), tg = it / (HD / 2);
+        const int t = tg / groups, h0 = (tg - t * groups) * kQkvHeads;
+        int d0, d1;
+        rope_slot_dims(c, tb, d0, d1);
+        const bool rot = c < tb.half;
+        float cs = 0.f, sn = 0.f;
+        if (rot) rope_cs_tab(pos[t], c, tb, cs, sn);
+        const int h1 = h0 + kQkvHeads < n_head ? h0 + kQkvHeads : n_head;
+        for (int h = h0; h < h1; ++h) {
+            const int r = t * n_head + h;
+            const float x0 = q32[r * HD + d0], x1 = q32[r * HD + d1];
+            const float y0 = rot ? rope_lo(x0, x1, cs, sn, tb.q_scale) : __fmul_rn(x0, tb.q_scale);
+            const float y1 = rot ? rope_hi(x0, x1, cs, sn, tb.q_scale) : __fmul_rn(x1, tb.q_scale);
+            unsigned char* row = tile + r * 128;
+            *reinterpret_cast<__half*>(row + (d0 >> 6) * q_box + ((((d0 & 63) >> 3) ^ (r & 7)) << 4) + (d0 & 7) * 2) =
+                __float2half_rn(y0);
+            *reinterpret_cast<__half*>(row + (d1 >> 6) * q_box + ((((d1 & 63) >> 3) ^ (r & 7)) << 4) + (d1 & 7) * 2) =
+                __float2half_rn(y1);
+        }
+    }
+}
+
+// Copy of the RoPE table into shared memory by threads [0, nthreads).
+__device__ __forceinline__ void copy_rope_table(RopeTable& dst, const RopeTable& src, int tid, int nthreads) {
+    for (int c = tid; c < kMaxPairs; c += nthreads) {
+        dst.turns[c] = src.turns[c];
+        dst.mix[c] = src.mix[c];
+        dst.ff[c] = src.ff[c];
+    }
+    if (tid == 0) {
+        dst.mscale = src.mscale;
+        dst.q_scale = src.q_scale;
+        dst.theta_scale = src.theta_scale;
+        dst.freq_scale = src.freq_scale;
+        dst.half = src.half;
+        dst.n_dims = src.n_dims;
+        dst.mode = src.mode;
+        dst.yarn = src.yarn;
+    }
+}
+
 inline bool aligned16(const void* p) { return (((uintptr_t)p) & 15u) == 0; }
 
 // Host: p is device memory of GPU `dev` (or managed memory). A host pointer,

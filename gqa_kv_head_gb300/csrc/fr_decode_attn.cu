@@ -424,21 +424,24 @@ static bool sw_shape_ok(int n_tok, int n_head, int hd) {
 // its in-launch merge.
 static constexpr int kSwAutoRows = 32;
 static constexpr int kSwAutoKeys = 1024;
-static bool use_sw(int n_tok, int n_head, int hd, int n_kv, const fr_attn_opts& o) {
-    if (o.engine != 0 || !sw_shape_ok(n_tok, n_head, hd)) return false;
-    if (o.layout == 2) return true;
-    if (o.layout == 1 || o.force_cluster != 0 || o.merge_mode == 1) return false;
+// Kernel of a call: 1 = 128-row query tiles (fr_attn_tc.cu, or the mma.sync
+// engine), 2 = keys on M (fr_attn_sw.cu). A forced layout 2 is validated by
+// the caller.
+static int pick_layout(int n_tok, int n_head, int hd, int n_kv, const fr_attn_opts& o) {
+    if (o.engine != 0) return 1;
+    if (o.layout == 2) return 2;
+    if (o.layout == 1 || o.force_cluster != 0 || o.merge_mode == 1) return 1;
     const int M = n_tok * n_head;
-    return M <= kSwAutoRows && n_kv >= kSwAutoKeys && n_kv >= 256 * M;
+    if (sw_shape_ok(n_tok, n_head, hd) && M <= kSwAutoRows && n_kv >= kSwAutoKeys && n_kv >= 256 * M) return 2;
+    return 1;
 }
-
 // Smallest workspace the plan a call with these options takes accepts: the
 // keys-on-M kernel needs only the header and the f16 Q slot (it cuts its split
 // count to what the workspace holds); the 128-row kernel its in-launch merge
 // plan; the mma.sync engine's needs count for the shapes it takes.
 static size_t workspace_bytes_for(int n_tok, int n_head, int hd, int n_kv, const fr_attn_opts& o) {
     const int M = n_tok * n_head;
-    if (use_sw(n_tok, n_head, hd, n_kv, o)) return kWsHeader + tc_q16_bytes(M, hd);
+    if (pick_layout(n_tok, n_head, hd, n_kv, o) != 1) return kWsHeader + tc_q16_bytes(M, hd);
     const size_t b = tc_workspace_bytes(M, hd);
     if (!decode_shape(n_tok, n_head)) return b;
     const size_t a = v1_workspace_bytes(M, hd, n_kv);
@@ -623,7 +626,7 @@ static fr_status decode_attn_impl(const uint16_t* q16, const float* q, int64_t q
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return FR_ERR_CUDA;
     unsigned char* w = static_cast<unsigned char*>(ws);
 
-    if (use_sw(n_tok, n_head, hd, n_kv, o)) {
+    if (pick_layout(n_tok, n_head, hd, n_kv, o) == 2) {
         const SwPlan p = make_sw_plan(M, hd, n_kv, sms, o.force_splits, ws_bytes);
         sw::SwLaunch L;
         memset(&L, 0, sizeof(L));
@@ -799,7 +802,8 @@ extern "C" fr_status fr_decode_attn_plan(int n_tok, int n_head, int hd, int n_kv
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return FR_ERR_CUDA;
     memset(plan, 0, sizeof(*plan));
     plan->engine = o.engine;
-    if (use_sw(n_tok, n_head, hd, n_kv, o)) {
+    plan->layout = pick_layout(n_tok, n_head, hd, n_kv, o);
+    if (plan->layout == 2) {
         const SwPlan p = make_sw_plan(M, hd, n_kv, sms, o.force_splits, workspace_bytes);
         plan->row_tiles = 1;
         plan->splits = p.splits;
@@ -821,8 +825,9 @@ extern "C" fr_status fr_decode_attn_plan(int n_tok, int n_head, int hd, int n_kv
         plan->cluster = 1;
         plan->merge_kernel = 0;
     }
-    // the keys-on-M kernel ropes the Q rows itself: no separate qkv_post launch
-    plan->launches = (fused_qkv_post && o.engine == 0 && !plan->keys_on_m ? 1 : 0) + 1 + plan->merge_kernel;
+    // the keys-on-M kernel (layout 2) ropes the Q rows itself: no separate
+    // qkv_post launch
+    plan->launches = (fused_qkv_post && o.engine == 0 && plan->layout == 1 ? 1 : 0) + 1 + plan->merge_kernel;
     return FR_OK;
 }
 

@@ -177,7 +177,7 @@ def decode_attn_plan(n_tok, n_head, hd, n_kv, *, fused_qkv_post=True, workspace_
                      splits=None, cluster=None, engine=None, merge_mode=None, layout=None):
     """fr_decode_attn_plan: the launch shape a call with these arguments would
     use on the current device (nothing is launched). Returns a dict with
-    engine, row_tiles, splits, cluster, merge_kernel, launches, keys_on_m."""
+    engine, row_tiles, splits, cluster, merge_kernel, launches, keys_on_m, layout."""
     lib = _abi.load()
     if workspace_bytes is None:
         workspace_bytes = workspace_size(n_tok, n_head, hd, n_kv)

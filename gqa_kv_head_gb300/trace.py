@@ -13,7 +13,7 @@ first CTA's set-up; medians over CTAs, and one CTA's tiles). Needs a GPU.
 import math
 import sys
 
-TRACE_OFFSET = 32 << 20          # FR_TRACE_OFFSET in csrc/fr_attn_sw.cu
+TRACE_OFFSET = 32 << 20          # FR_TRACE_OFFSET in csrc/fr_trace.cuh
 SLOTS = 64
 
 
@@ -27,9 +27,10 @@ def main(argv):
     from . import ops
     import gen
 
+    layout = 2
     for name in argv:
         w = gen.make_workload(name)
-        plan = ops.decode_attn_plan(w.n_tok, w.n_head, w.hd, w.n_kv, layout=2,
+        plan = ops.decode_attn_plan(w.n_tok, w.n_head, w.hd, w.n_kv, layout=layout,
                                     workspace_bytes=TRACE_OFFSET)
         n_rep = max(2, math.ceil(2 * 135e6 / (4 * w.n_kv * w.hd)))
         reps = [dict(q=torch.from_numpy(w.q()).cuda(), pos=torch.from_numpy(w.pos()).cuda(),
@@ -43,7 +44,7 @@ def main(argv):
         def call(i):
             r = reps[i % n_rep]
             ops.decode_attn(r["k"], r["v"], w.n_tok, w.n_head, q=r["q"], pos=r["pos"], rope=w.rope,
-                            mask=r["mask"], out=out, workspace=ws[:TRACE_OFFSET], stream=st, layout=2)
+                            mask=r["mask"], out=out, workspace=ws[:TRACE_OFFSET], stream=st, layout=layout)
 
         with torch.cuda.stream(st):
             for i in range(4):

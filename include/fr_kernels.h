@@ -281,6 +281,8 @@ typedef struct fr_attn_plan {
     int merge_kernel;      /* 1: split states merged by a separate kernel */
     int launches;          /* kernels one call launches (qkv_post, attention, merge) */
     int keys_on_m;         /* 1: 128-key tiles are the MMA's M, the query rows its N */
+    int layout;            /* kernel: 1 = 128-row query tiles, 2 = keys on M (see
+                              fr_attn_opts.layout) */
 } fr_attn_plan;
 
 fr_status fr_decode_attn_plan(int n_tok, int n_head, int hd, int n_kv, int fused_qkv_post,

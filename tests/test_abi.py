@@ -44,7 +44,7 @@ def test_status_strings_and_version(lib):
     assert lib.fr_status_string(0) == b"FR_OK"
     for s in range(1, 6):
         assert lib.fr_status_string(s).startswith(b"FR_ERR_")
-    assert lib.fr_abi_version() >> 16 == 2
+    assert lib.fr_abi_version() >> 16 == 3
 
 
 def test_workspace_size_host_logic(lib):
