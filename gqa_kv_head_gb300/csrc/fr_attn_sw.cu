@@ -37,8 +37,10 @@
 // In the fused call the kernel ropes the Q rows itself with qkv_post's
 // arithmetic (fr_qkv_post's device routines), so one call is one launch.
 // Each split writes its unnormalised O rows with its row maxima (log2 units)
-// and sums to the workspace, and attn_merge_kernel combines them; a single
-// split normalises and writes the output rows itself.
+// and sums to the workspace (part_o[s][r][hd]: a split's rows are contiguous);
+// after a bounded grid barrier (cooperative launch) the softmax warps of every
+// CTA merge a share of the output rows. A single split normalises and writes
+// the output rows itself.
 // Every mbarrier wait is bounded; a wait that gives up sets the status word,
 // and the CTA still drains its copies and MMAs and frees its TMEM.
 #include <math.h>
@@ -62,6 +64,7 @@ constexpr float kTau = 8.0f;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr int kBox = 16384;              // 128 rows x 128 bytes (64 f16), 128-byte swizzle
 constexpr int kStage = 2 * kBox;         // 128 keys x 128 dims of K or V
+constexpr int kPrefetchPieces = 2;       // ring pieces prefetched to L2 before the launch wait
 constexpr int kSmemLimit = 232448;
 
 template <int HD, int NQ>
@@ -323,7 +326,8 @@ attn_sw_kernel(const __grid_constant__ SwArgs a, const __grid_constant__ SwMaps 
             };
             // While the grid ahead finishes, the first inputs are prefetched into
             // L2 (a prefetch returns no data, so it may precede the wait below):
-            // the Q rows, the first mask tiles and the first ring's K/V stages.
+            // the Q rows, the first mask tiles and the first K tile (more K/V
+            // prefetches from every CTA would queue ahead of the Q rows).
             if (a.rope_in_kernel)
                 for (int t = 0; t < a.n_tok; ++t)
                     bulk_prefetch_l2(a.q + (int64_t)t * a.q_tok_stride, (uint32_t)(a.n_head * HD * 4));
@@ -331,7 +335,7 @@ attn_sw_kernel(const __grid_constant__ SwArgs a, const __grid_constant__ SwMaps 
                 tma_prefetch_2d(&mp.mask, k_begin + i * kKeys, 0);
                 tma_prefetch_2d(&mp.mask, k_begin + i * kKeys + 64, 0);
             }
-            for (int p = 0; p < min(C::R, n_pieces); ++p) {
+            for (int p = 0; p < min(kPrefetchPieces, n_pieces); ++p) {
                 const int u = p / C::HALVES, h = p - u * C::HALVES;
                 const bool is_v = u == n_units - 1 || (u > 0 && !(u & 1));
                 const int tile = u == 0 ? 0 : (u == n_units - 1 ? n_my - 1 : ((u & 1) ? (u + 1) >> 1 : (u >> 1) - 1));
@@ -356,13 +360,11 @@ attn_sw_kernel(const __grid_constant__ SwArgs a, const __grid_constant__ SwMaps 
                 for (int b = 0; b < HD / 64; ++b)
                     tma_load_2d(smem_addr(sm + C::Q_OFF + b * C::Q_BOX), &mp.q16, b * 64, 0, bar(C::B_QFULL));
             }
-            // the Q rows and the first mask tiles first, on their own: issued
-            // together with every CTA's first K/V stages they would queue behind
-            // tens of MB of requests, and the first tile needs them (issuing the
-            // first K tile with them measured no faster)
+            // the Q rows and the first mask tiles first (ahead of every K/V
+            // request in the queues), then the whole ring at once: its first fill
+            // overlaps the Q rows' latency and their RoPE
             int np = 0, nm = 0;
             for (; nm < min(C::MS, n_masks); ++nm) load_mask(nm);
-            if (!mbar_wait(bar(a.rope_in_kernel ? C::B_QF32 : C::B_QFULL), 0, limit)) record_timeout(a.status, 1u);
             for (; np < min(C::R, n_pieces); ++np) load_piece(np);
             uint64_t t_last = global_ns();
             while (np < n_pieces || nm < n_masks) {
@@ -792,6 +794,7 @@ attn_sw_kernel(const __grid_constant__ SwArgs a, const __grid_constant__ SwMaps 
     tc_fence_before();
     __syncthreads();
     if (tid == 0) FR_STAMP(2);                   // done
+    if (a.splits > 1 && tid == 0) split_merge::grid_barrier_depart(a.barrier, (unsigned)a.splits);
     if (warp == kMmaWarp) {
         __syncwarp();
         tc_fence_after();

@@ -24,28 +24,29 @@ __device__ __forceinline__ unsigned ld_acquire_u32(const unsigned* p) {
 
 // One thread per CTA, after the CTA's state is stored (and a CTA barrier):
 // arrive with a release add (the state is visible before the count moves),
-// then poll the count until every one of the n CTAs has arrived; the last CTA
-// to leave returns both words to zero for the next call (whose CTAs arrive
-// only after this grid is complete). Every CTA must be resident (cooperative
-// launch). Returns false if the wait gave up after limit_ns.
+// then poll the count until every one of the n CTAs has arrived. Every CTA
+// must be resident (cooperative launch). Returns false if the wait gave up
+// after limit_ns. Each CTA calls grid_barrier_depart once it no longer needs
+// the barrier (off the critical path, at its end): the last to depart returns
+// both words to zero for the next call, whose CTAs arrive only after this grid
+// is complete.
 __device__ __forceinline__ bool grid_barrier(unsigned* barrier, unsigned n, uint64_t limit_ns) {
     unsigned* count = barrier;
-    unsigned* departed = barrier + 1;
     red_release_add_u32(count, 1u);
     const uint64_t t_start = global_ns();
-    bool ok = true;
     while (ld_acquire_u32(count) < n) {
-        if (global_ns() - t_start > limit_ns) {
-            ok = false;
-            break;
-        }
+        if (global_ns() - t_start > limit_ns) return false;
         __nanosleep(20);
     }
+    return true;
+}
+__device__ __forceinline__ void grid_barrier_depart(unsigned* barrier, unsigned n) {
+    unsigned* count = barrier;
+    unsigned* departed = barrier + 1;
     if (atomicAdd(departed, 1u) == n - 1u) {
         *count = 0u;
         *departed = 0u;
     }
-    return ok;
 }
 
 }  // namespace split_merge
