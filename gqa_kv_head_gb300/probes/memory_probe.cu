@@ -9,6 +9,10 @@
 //            one warp per CTA reads one 128-byte line of 20 other CTAs'
 //            blocks (independent loads) and times them; then 20 more lines
 //            of the same blocks (the lines are warm).
+//   dsmem    clusters of 2 or 8 CTAs: every CTA pushes 96 KiB into the shared
+//            memory of the next CTA of its cluster with 16-byte
+//            st.shared::cluster stores (all 256 threads), then a cluster
+//            barrier; the push time per CTA gives GB/s per SM.
 // Every wait is bounded (0.2 s); a wait that gives up sets a status bit that
 // the host prints. Build and run: python -m gqa_kv_head_gb300.probes
 #include <cuda.h>
@@ -120,6 +124,56 @@ __global__ void __launch_bounds__(256) fresh_kernel(float* states, unsigned* bar
     }
 }
 
+constexpr int kPushBytes = 96 * 1024;
+
+__global__ void __launch_bounds__(256, 1) dsmem_kernel(unsigned long long* out) {
+    extern __shared__ __align__(16) unsigned char buf[];
+    const uint32_t rank = cluster_rank(), n = cluster_nrank();
+    const uint32_t peer = (rank + 1) % n;
+    cluster_sync();                                         // every CTA of the cluster is running
+    const uint64_t t0 = global_ns();
+    const uint32_t base = map_rank(smem_addr(buf), peer);
+    for (int i = threadIdx.x; i < kPushBytes / 16; i += blockDim.x)
+        st_cluster_v4(base + i * 16, make_uint4(i, rank, 0u, 0u));
+    cluster_sync();                                         // every push has landed
+    const uint64_t t1 = global_ns();
+    if (threadIdx.x == 0) out[blockIdx.x] = t1 - t0;
+}
+
+static void run_dsmem(int cluster, unsigned long long* out) {
+    const int ctas = 152 / cluster * cluster;
+    cudaFuncSetAttribute(dsmem_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kPushBytes);
+    cudaFuncSetAttribute(dsmem_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    cudaLaunchConfig_t cfg;
+    memset(&cfg, 0, sizeof(cfg));
+    cfg.gridDim = dim3(ctas);
+    cfg.blockDim = dim3(256);
+    cfg.dynamicSmemBytes = kPushBytes;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = cluster;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    double sum = 0;
+    const int reps = 4;
+    for (int it = 0; it < reps; ++it) {
+        if (cudaLaunchKernelEx(&cfg, dsmem_kernel, out) != cudaSuccess) {
+            printf("dsmem cluster %d: launch failed (%s)\n", cluster, cudaGetErrorString(cudaGetLastError()));
+            return;
+        }
+        cudaDeviceSynchronize();
+        unsigned long long h[152];
+        cudaMemcpy(h, out, ctas * 8, cudaMemcpyDeviceToHost);
+        if (it == 0) continue;
+        for (int i = 0; i < ctas; ++i) sum += h[i];
+    }
+    const double ns = sum / ((double)ctas * (reps - 1));
+    printf("DSMEM push, clusters of %d (%3d CTAs): %.0f ns for %d KiB per CTA = %.1f GB/s per SM (%s)\n", cluster,
+           ctas, ns, kPushBytes / 1024, kPushBytes / ns, cudaGetErrorString(cudaGetLastError()));
+}
+
 static PFN_cuTensorMapEncodeTiled_v12000 encoder() {
     static PFN_cuTensorMapEncodeTiled_v12000 f = nullptr;
     if (!f) {
@@ -213,6 +267,8 @@ int main() {
             wait += h[3 * i + 2];
         }
     }
+    run_dsmem(2, out);
+    run_dsmem(8, out);
     const double cnt = (double)n * (reps - 1);
     unsigned st = 0;
     cudaMemcpy(&st, status, 4, cudaMemcpyDeviceToHost);
