@@ -34,13 +34,13 @@ class FrRopeParams(ctypes.Structure):
 class FrAttnOpts(ctypes.Structure):
     _fields_ = [("engine", ctypes.c_int), ("force_splits", ctypes.c_int),
                 ("force_cluster", ctypes.c_int), ("wait_probe_iters", ctypes.c_int),
-                ("merge_mode", ctypes.c_int), ("layout", ctypes.c_int)]
+                ("merge_mode", ctypes.c_int), ("layout", ctypes.c_int), ("slice_rows", ctypes.c_int)]
 
 
 class FrAttnPlan(ctypes.Structure):
     _fields_ = [("engine", ctypes.c_int), ("row_tiles", ctypes.c_int), ("splits", ctypes.c_int),
                 ("cluster", ctypes.c_int), ("merge_kernel", ctypes.c_int), ("launches", ctypes.c_int),
-                ("keys_on_m", ctypes.c_int), ("layout", ctypes.c_int)]
+                ("keys_on_m", ctypes.c_int), ("layout", ctypes.c_int), ("row_slices", ctypes.c_int)]
 
 
 _P = ctypes.c_void_p

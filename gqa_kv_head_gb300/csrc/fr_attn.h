@@ -64,7 +64,8 @@ fr_status launch_merge(const float* part_o, const float2* part_ml, float* out, i
 // (fr_attn_sw.cu): one KV split per CTA.
 namespace sw {
 
-constexpr int kMaxRows = 64;
+constexpr int kMaxRows = 128;            // M over all slices
+constexpr int kMaxSliceRows = 64;        // NQ, the MMA's N
 
 struct SwArgs {
     float* out;
@@ -78,7 +79,8 @@ struct SwArgs {
     int has_mask;
     int n_tok, n_head, M, n_kv;
     int keys_per_split;       // a multiple of 16; split s reads keys [s*kps, min(n_kv, (s+1)*kps))
-    int splits;
+    int splits;               // KV splits (states per row)
+    int slices;               // row slices per split: CTA b takes split b / slices, rows [(b % slices)*NQ, +NQ)
     int rstride;              // rows per split block of part_o / part_ml (= M)
     unsigned* barrier;        // [2]: arrival and departure counts (grid barrier before the merge)
     int early_dep;            // 1: the grid is one wave; a dependent launch may start after set-up
@@ -102,9 +104,10 @@ struct SwLaunch {
     int64_t k_rs, v_rs, m_rs;
 };
 
-// N of the MMA (query rows padded to 16, 32 or 64).
+// N of the MMA (query rows padded to 16, 32 or 64) for a slice of M rows.
 int rows_n(int M);
-fr_status launch_sw(const SwLaunch& L, int hd, cudaStream_t stream);
+// nq: rows per slice (16, 32 or 64); the grid is args.splits * args.slices.
+fr_status launch_sw(const SwLaunch& L, int hd, int nq, cudaStream_t stream);
 
 }  // namespace sw
 

@@ -10,7 +10,10 @@
 // padding; here 128 keys are the MMA's M and the query rows its N (16, 32 or
 // 64), so the tensor work follows the real rows.
 //
-// One CTA = one KV split (one CTA per SM); W softmax warps (8 for 16 rows,
+// One CTA = one KV split x one slice of NQ query rows (one CTA per SM; with
+// more than 64 rows, or when the plan asks for it, the rows are cut into
+// slices whose CTAs read the same K/V tiles, the later reads served by L2);
+// W softmax warps (8 for 16 rows,
 // 16 for 32 or 64 rows) and two more:
 //   warps 0..W-1  softmax, one thread per (key of the tile, W/4-th of the
 //              query rows): warps w, w + 4, ... share TMEM lane quadrant w % 4
@@ -227,7 +230,9 @@ attn_sw_kernel(const __grid_constant__ SwArgs a, const __grid_constant__ SwMaps 
     int* sFlag = reinterpret_cast<int*>(sm + C::AUX_OFF + C::AUX_FLAG);       // some row's reference grew
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int split = blockIdx.x;
+    const int split = blockIdx.x / a.slices;                        // KV split
+    const int r_lo = (blockIdx.x - split * a.slices) * NQ;          // this CTA's query rows [r_lo, r_lo + r_n)
+    const int r_n = min(NQ, a.M - r_lo);
     const int k_begin = split * a.keys_per_split;                   // this split's keys
     const int k_end = min(a.n_kv, k_begin + a.keys_per_split);
     const int n_my = k_end > k_begin ? (k_end - k_begin + kKeys - 1) / kKeys : 0;   // tiles (the last may be short)
@@ -328,9 +333,18 @@ attn_sw_kernel(const __grid_constant__ SwArgs a, const __grid_constant__ SwMaps 
             // L2 (a prefetch returns no data, so it may precede the wait below):
             // the Q rows, the first mask tiles and the first K tile (more K/V
             // prefetches from every CTA would queue ahead of the Q rows).
+            // this slice's rows of token t: heads [max(0, r_lo - t*n_head), min(n_head, r_lo + r_n - t*n_head))
+            const int t_lo = r_lo / a.n_head, t_hi = (r_lo + r_n - 1) / a.n_head;
+            auto q_run = [&](int t, int& h_a, int& h_b) {
+                h_a = max(0, r_lo - t * a.n_head);
+                h_b = min(a.n_head, r_lo + r_n - t * a.n_head);
+            };
             if (a.rope_in_kernel)
-                for (int t = 0; t < a.n_tok; ++t)
-                    bulk_prefetch_l2(a.q + (int64_t)t * a.q_tok_stride, (uint32_t)(a.n_head * HD * 4));
+                for (int t = t_lo; t <= t_hi; ++t) {
+                    int h_a, h_b;
+                    q_run(t, h_a, h_b);
+                    bulk_prefetch_l2(a.q + (int64_t)t * a.q_tok_stride + (int64_t)h_a * HD, (uint32_t)((h_b - h_a) * HD * 4));
+                }
             for (int i = 0; i < min(C::MS, n_masks); ++i) {
                 tma_prefetch_2d(&mp.mask, k_begin + i * kKeys, 0);
                 tma_prefetch_2d(&mp.mask, k_begin + i * kKeys + 64, 0);
@@ -349,16 +363,22 @@ attn_sw_kernel(const __grid_constant__ SwArgs a, const __grid_constant__ SwMaps 
             asm volatile("griddepcontrol.wait;" ::: "memory");
             FR_STAMP(4);                         // the grids ahead are complete
             if (a.rope_in_kernel) {
-                // the f32 Q rows, one bulk copy per token (its n_head rows are contiguous)
-                const uint32_t row_bytes = (uint32_t)(a.n_head * HD * 4);
-                mbar_expect_tx(bar(C::B_QF32), row_bytes * (uint32_t)a.n_tok);
-                for (int t = 0; t < a.n_tok; ++t)
-                    bulk_load(smem_addr(sm + C::P_OFF + t * row_bytes), a.q + (int64_t)t * a.q_tok_stride, row_bytes,
+                // this slice's f32 Q rows, one bulk copy per token (a token's
+                // heads are contiguous), staged as rows [0, r_n)
+                mbar_expect_tx(bar(C::B_QF32), (uint32_t)(r_n * HD * 4));
+                for (int t = t_lo; t <= t_hi; ++t) {
+                    int h_a, h_b;
+                    q_run(t, h_a, h_b);
+                    bulk_load(smem_addr(sm + C::P_OFF + (t * a.n_head + h_a - r_lo) * HD * 4),
+                              a.q + (int64_t)t * a.q_tok_stride + (int64_t)h_a * HD, (uint32_t)((h_b - h_a) * HD * 4),
                               bar(C::B_QF32));
+                }
             } else {
+                // rows [r_lo, r_lo + NQ) of the f16 rows: past M the copy reads
+                // zeros; rows of the next slice are masked out below
                 mbar_expect_tx(bar(C::B_QFULL), (uint32_t)C::Q_BYTES);
                 for (int b = 0; b < HD / 64; ++b)
-                    tma_load_2d(smem_addr(sm + C::Q_OFF + b * C::Q_BOX), &mp.q16, b * 64, 0, bar(C::B_QFULL));
+                    tma_load_2d(smem_addr(sm + C::Q_OFF + b * C::Q_BOX), &mp.q16, b * 64, r_lo, bar(C::B_QFULL));
             }
             // the Q rows and the first mask tiles first (ahead of every K/V
             // request in the queues), then the whole ring at once: its first fill
@@ -479,8 +499,8 @@ attn_sw_kernel(const __grid_constant__ SwArgs a, const __grid_constant__ SwMaps 
             int* sPos = reinterpret_cast<int*>(sm + C::AUX_OFF + C::AUX_POS);
             if (tid < a.n_tok) sPos[tid] = __ldg(a.pos + tid);
             unsigned char* sQ = sm + C::Q_OFF;
-            for (int i = tid; i < (NQ - a.M) * (HD / 8); i += kSmaxThreads) {      // zero rows [M, NQ)
-                const int r = a.M + i / (HD / 8), ch = i % (HD / 8);
+            for (int i = tid; i < (NQ - r_n) * (HD / 8); i += kSmaxThreads) {      // zero rows [r_n, NQ)
+                const int r = r_n + i / (HD / 8), ch = i % (HD / 8);
                 *reinterpret_cast<uint4*>(sQ + (ch >> 3) * C::Q_BOX + r * 128 + ((ch & 7) << 4)) =
                     make_uint4(0u, 0u, 0u, 0u);
             }
@@ -488,7 +508,7 @@ attn_sw_kernel(const __grid_constant__ SwArgs a, const __grid_constant__ SwMaps 
             if (tid == 0) FR_STAMP(5);
             wait(bar(C::B_QF32), 0);
             if (tid == 0) FR_STAMP(6);           // the f32 Q rows have landed
-            rope_rows_to_tile<HD>(reinterpret_cast<const float*>(sm + C::P_OFF), sPos, stb, a.n_tok, a.n_head, sQ,
+            rope_rows_to_tile<HD>(reinterpret_cast<const float*>(sm + C::P_OFF), sPos, stb, a.n_head, r_lo, r_n, sQ,
                                   C::Q_BOX, tid, kSmaxThreads);
             if (tid == 0) FR_STAMP(7);               // rows roped
             softmax_bar_sync<kSmaxThreads>();                  // every f32 row read: the P buffers are free again
@@ -512,7 +532,8 @@ attn_sw_kernel(const __grid_constant__ SwArgs a, const __grid_constant__ SwMaps 
         for (int w4 = 0; w4 < (RH + 3) / 4; ++w4) {
             uint32_t pk = 0;
 #pragma unroll
-            for (int u = 0; u < 4; ++u) pk |= (uint32_t)min((r0 + w4 * 4 + u) / a.n_head, a.n_tok - 1) << (8 * u);
+            for (int u = 0; u < 4; ++u)
+                pk |= (uint32_t)min((r_lo + r0 + w4 * 4 + u) / a.n_head, a.n_tok - 1) << (8 * u);
             tokp[w4] = pk;
         }
         const int rb = rs_row<RH>(lane);
@@ -551,7 +572,7 @@ attn_sw_kernel(const __grid_constant__ SwArgs a, const __grid_constant__ SwMaps 
             bool over = false;
 #pragma unroll
             for (int u = 0; u < RH; ++u) {
-                if (!key_ok || r0 + u >= a.M) x[u] = -INFINITY;
+                if (!key_ok || r0 + u >= r_n) x[u] = -INFINITY;
                 over |= x[u] > mref[u] + kTau;           // -inf + tau = -inf: a first finite score counts
             }
             // the row references change only when some score exceeds its row's
@@ -653,7 +674,7 @@ attn_sw_kernel(const __grid_constant__ SwArgs a, const __grid_constant__ SwMaps 
         if (tid == 0) FR_STAMP(57);              // row sums reduced
         // ---- epilogue: O = O_hi + O_lo; this thread's lane is head dim k of
         // each half, its rows [r0, r0 + RH)
-        const int rows = a.M;
+        const int rows = r_n;
         const bool single = a.splits == 1;
         constexpr int EC = RH < 16 ? RH : 16;            // columns per TMEM read
 #pragma unroll 1
@@ -678,16 +699,16 @@ attn_sw_kernel(const __grid_constant__ SwArgs a, const __grid_constant__ SwMaps 
                         const float o = hi[u] + lo[u];
                         if (single) {
                             const float L = sL[r];
-                            a.out[(int64_t)r * HD + d] = L > 0.f ? o / L : 0.f;
+                            a.out[(int64_t)(r_lo + r) * HD + d] = L > 0.f ? o / L : 0.f;
                         } else {
-                            a.part_o[((int64_t)split * a.rstride + r) * HD + d] = o;
+                            a.part_o[((int64_t)split * a.rstride + r_lo + r) * HD + d] = o;
                         }
                     }
                 }
             }
         }
         if (!single && tid < rows)
-            a.part_ml[(int64_t)split * a.rstride + tid] =
+            a.part_ml[(int64_t)split * a.rstride + r_lo + tid] =
                 n_my > 0 ? make_float2(sM[tid], sL[tid]) : make_float2(-INFINITY, 0.f);
         if (tid == 0) FR_STAMP(58);              // rows stored
     }
@@ -702,7 +723,7 @@ attn_sw_kernel(const __grid_constant__ SwArgs a, const __grid_constant__ SwMaps 
         __syncthreads();                         // this CTA's state is stored
         if (tid == 0) {
             FR_STAMP(59);
-            if (!split_merge::grid_barrier(a.barrier, (unsigned)a.splits, limit)) record_timeout(a.status, 4u);
+            if (!split_merge::grid_barrier(a.barrier, gridDim.x, limit)) record_timeout(a.status, 4u);
         }
         __syncthreads();
         if (tid == 0) FR_STAMP(56);              // every split's state stored
@@ -717,8 +738,9 @@ attn_sw_kernel(const __grid_constant__ SwArgs a, const __grid_constant__ SwMaps 
             // one chunk covers a warp's share whenever G = every softmax warp
             constexpr int CHUNK = (tc::kMaxMergeSplits + kSmaxWarps - 1) / kSmaxWarps;
             const int units = a.M * NCH;
-            const int S = a.splits;
-            const int per = (S * kSmaxWarps) / units;          // warps of the grid per unit
+            const int S = a.splits;                             // states per row
+            const int n_cta = gridDim.x;                        // merging CTAs
+            const int per = (n_cta * kSmaxWarps) / units;      // warps of the grid per unit
             int G = 1;
             while (G * 2 <= kSmaxWarps && G * 2 <= per) G *= 2;
             const int groups = kSmaxWarps / G;                  // per CTA
@@ -726,9 +748,9 @@ attn_sw_kernel(const __grid_constant__ SwArgs a, const __grid_constant__ SwMaps 
             float* sAcc = reinterpret_cast<float*>(sm + C::RING_OFF);     // [warps][32] (the ring is idle)
             float* sMw = sAcc + kSmaxWarps * 32;                        // [warps]
             float* sLw = sMw + kSmaxWarps;                              // [warps]
-            const int rounds = (units + S * groups - 1) / (S * groups); // the same for every warp
+            const int rounds = (units + n_cta * groups - 1) / (n_cta * groups); // the same for every warp
             for (int rd = 0; rd < rounds; ++rd) {
-                const int u = (rd * S + split) * groups + gi;
+                const int u = (rd * n_cta + (int)blockIdx.x) * groups + gi;
                 const bool live = u < units;
                 const int r = live ? u / NCH : 0, c0 = live ? (u - (u / NCH) * NCH) * 32 : 0;
                 float mx = -INFINITY, acc = 0.f, L = 0.f;
@@ -794,7 +816,7 @@ attn_sw_kernel(const __grid_constant__ SwArgs a, const __grid_constant__ SwMaps 
     tc_fence_before();
     __syncthreads();
     if (tid == 0) FR_STAMP(2);                   // done
-    if (a.splits > 1 && tid == 0) split_merge::grid_barrier_depart(a.barrier, (unsigned)a.splits);
+    if (a.splits > 1 && tid == 0) split_merge::grid_barrier_depart(a.barrier, gridDim.x);
     if (warp == kMmaWarp) {
         __syncwarp();
         tc_fence_after();
@@ -831,7 +853,7 @@ static fr_status launch(const SwLaunch& L, cudaStream_t stream) {
         return FR_ERR_CUDA;
     cudaLaunchConfig_t cfg;
     memset(&cfg, 0, sizeof(cfg));
-    cfg.gridDim = dim3(a.splits, 1, 1);
+    cfg.gridDim = dim3(a.splits * a.slices, 1, 1);
     cfg.blockDim = dim3(Cfg<HD, NQ>::THREADS, 1, 1);
     cfg.dynamicSmemBytes = Cfg<HD, NQ>::SMEM;
     cfg.stream = stream;
@@ -857,8 +879,7 @@ static fr_status launch(const SwLaunch& L, cudaStream_t stream) {
 
 int rows_n(int M) { return M <= 16 ? 16 : (M <= 32 ? 32 : 64); }
 
-fr_status launch_sw(const SwLaunch& L, int hd, cudaStream_t stream) {
-    const int nq = rows_n(L.args.M);
+fr_status launch_sw(const SwLaunch& L, int hd, int nq, cudaStream_t stream) {
     if (hd == 128) {
         if (nq == 16) return launch<128, 16>(L, stream);
         if (nq == 32) return launch<128, 32>(L, stream);

@@ -142,28 +142,33 @@ __device__ __forceinline__ void rope_slot(const float* __restrict__ qrow, int c,
     rope_slot_apply(c, qrow[d0], qrow[d1], pos, tb, y0, y1);
 }
 
-// The f16 Q tile of an attention kernel that ropes its own rows: row
-// r = t*n_head + h (t-major, the order qkv_post emits) from the f32 rows
-// staged in shared memory at q32[r*HD], written K-major in the 128-byte
-// swizzle (64 dims per box of q_box bytes, 128 bytes per row). One work item
-// is (token, slot, group of kQkvHeads heads) with one cos/sin, and every value
-// goes through rope_cs_tab / rope_lo / rope_hi like qkv_post's: the bits equal
-// its f16 rows. Called by threads [0, nthreads) with their index tid.
+// The f16 Q tile of an attention kernel that ropes its own rows: query rows
+// [r_lo, r_lo + r_n) (row r = t*n_head + h, t-major, the order qkv_post emits)
+// from the f32 rows staged in shared memory at q32[(r - r_lo)*HD], written as
+// tile rows r - r_lo, K-major in the 128-byte swizzle (64 dims per box of
+// q_box bytes, 128 bytes per row). One work item is (token, slot, group of
+// kQkvHeads heads) with one cos/sin, and every value goes through rope_cs_tab /
+// rope_lo / rope_hi like qkv_post's: the bits equal its f16 rows. Called by
+// threads [0, nthreads) with their index tid.
 template <int HD>
-__device__ __forceinline__ void rope_rows_to_tile(const float* q32, const int* pos, const RopeTable& tb, int n_tok,
-                                                  int n_head, unsigned char* tile, int q_box, int tid, int nthreads) {
+__device__ __forceinline__ void rope_rows_to_tile(const float* q32, const int* pos, const RopeTable& tb, int n_head,
+                                                  int r_lo, int r_n, unsigned char* tile, int q_box, int tid,
+                                                  int nthreads) {
     const int groups = (n_head + kQkvHeads - 1) / kQkvHeads;
-    for (int it = tid; it < n_tok * groups * (HD / 2); it += nthreads) {
+    const int t_lo = r_lo / n_head, n_t = (r_lo + r_n - 1) / n_head - t_lo + 1;
+    for (int it = tid; it < n_t * groups * (HD / 2); it += nthreads) {
         const int c = it % (HD / 2), tg = it / (HD / 2);
-        const int t = tg / groups, h0 = (tg - t * groups) * kQkvHeads;
+        const int t = t_lo + tg / groups, h0 = (tg % groups) * kQkvHeads;
+        const int ha = max(h0, r_lo - t * n_head);                      // heads of the group inside the rows
+        const int hb = min(min(h0 + kQkvHeads, n_head), r_lo + r_n - t * n_head);
+        if (ha >= hb) continue;
         int d0, d1;
         rope_slot_dims(c, tb, d0, d1);
         const bool rot = c < tb.half;
         float cs = 0.f, sn = 0.f;
         if (rot) rope_cs_tab(pos[t], c, tb, cs, sn);
-        const int h1 = h0 + kQkvHeads < n_head ? h0 + kQkvHeads : n_head;
-        for (int h = h0; h < h1; ++h) {
-            const int r = t * n_head + h;
+        for (int h = ha; h < hb; ++h) {
+            const int r = t * n_head + h - r_lo;                        // tile row
             const float x0 = q32[r * HD + d0], x1 = q32[r * HD + d1];
             const float y0 = rot ? rope_lo(x0, x1, cs, sn, tb.q_scale) : __fmul_rn(x0, tb.q_scale);
             const float y1 = rot ? rope_hi(x0, x1, cs, sn, tb.q_scale) : __fmul_rn(x1, tb.q_scale);

@@ -417,13 +417,29 @@ static size_t tc_merge_workspace_bytes(int M, int hd) {
 static bool sw_shape_ok(int n_tok, int n_head, int hd) {
     return (hd == 128 || hd == 256) && n_tok <= kMaskWin && (int64_t)n_tok * n_head <= sw::kMaxRows;
 }
-// The library's choice (measured on GB300, graph replay of fused calls): the
-// keys-on-M kernel wins by 10-25 % at up to 32 query rows when there are at
-// least 1024 keys and 256 per row; at 64 rows its softmax is slower than the
-// 128-row kernel's, and with fewer keys per row its short loop does not pay for
-// its in-launch merge.
-static constexpr int kSwAutoRows = 32;
-static constexpr int kSwAutoKeys = 1024;
+// The library's choice of the keys-on-M kernel and its slice size (measured
+// on GB300, graph replay of fused calls, against the 128-row kernel):
+//  (a) 16-row slices when the KV range is short: n_kv >= 1024 and
+//      ceil(M/16) * n_kv <= 16384 (each CTA then streams at most ~16384
+//      keys' worth of its split): 8-19 % faster at 1024-2048 keys for every
+//      M up to 128, even at the limit (4096 keys for 64 rows, 8192 for 32);
+//      beyond it the slices' repeated reads of each K/V tile cost more than
+//      they save, and below 1024 keys the 128-row kernel's short call wins;
+//  (b) one slice of all rows for M <= 32 and n_kv >= max(1024, 256 M):
+//      10-25 % faster on long KV;
+//  (c) 32-row slices for hd 128, 32 < M <= 64 and n_kv >= 16384: 3-7 %
+//      faster (two CTAs per split read each tile);
+// else the 128-row kernel. Returns the rows per slice, or 0 for layout 1.
+static constexpr int kSwShortKeys = 1024;
+static constexpr int64_t kSwShortWork = 16384;
+static int auto_sw_rows(int n_tok, int n_head, int hd, int n_kv) {
+    if (!sw_shape_ok(n_tok, n_head, hd)) return 0;
+    const int M = n_tok * n_head;
+    if (n_kv >= kSwShortKeys && (int64_t)((M + 15) / 16) * n_kv <= kSwShortWork) return 16;
+    if (M <= 32 && n_kv >= kSwShortKeys && n_kv >= 256 * M) return sw::rows_n(M);
+    if (hd == 128 && M > 32 && M <= 64 && n_kv >= 16384) return 32;
+    return 0;
+}
 // Kernel of a call: 1 = 128-row query tiles (fr_attn_tc.cu, or the mma.sync
 // engine), 2 = keys on M (fr_attn_sw.cu). A forced layout 2 is validated by
 // the caller.
@@ -431,10 +447,9 @@ static int pick_layout(int n_tok, int n_head, int hd, int n_kv, const fr_attn_op
     if (o.engine != 0) return 1;
     if (o.layout == 2) return 2;
     if (o.layout == 1 || o.force_cluster != 0 || o.merge_mode == 1) return 1;
-    const int M = n_tok * n_head;
-    if (sw_shape_ok(n_tok, n_head, hd) && M <= kSwAutoRows && n_kv >= kSwAutoKeys && n_kv >= 256 * M) return 2;
-    return 1;
+    return auto_sw_rows(n_tok, n_head, hd, n_kv) > 0 ? 2 : 1;
 }
+
 // Smallest workspace the plan a call with these options takes accepts: the
 // keys-on-M kernel needs only the header and the f16 Q slot (it cuts its split
 // count to what the workspace holds); the 128-row kernel its in-launch merge
@@ -539,10 +554,28 @@ static size_t sw_split_bytes(int M, int hd) { return (size_t)M * (hd * sizeof(fl
 // last tile may be short, its keys past the range masked.
 struct SwPlan {
     int splits, keys_per_split;
+    int nq, slices;        // rows per slice (the MMA's N) and slices per split
 };
 
-static SwPlan make_sw_plan(int M, int hd, int n_kv, int num_sms, int force_splits, size_t ws_bytes) {
+// Rows per slice: the caller's choice (16, 32 or 64), else the library's
+// (auto_sw_rows), else (layout 2 forced where the library would not pick it)
+// all rows in one slice up to 64 and 32-row slices beyond.
+static int sw_slice_rows(int n_tok, int n_head, int hd, int n_kv, const fr_attn_opts& o) {
+    if (o.slice_rows > 0) return o.slice_rows;
+    const int a = auto_sw_rows(n_tok, n_head, hd, n_kv);
+    if (a > 0) return a;
+    const int M = n_tok * n_head;
+    return M <= sw::kMaxSliceRows ? sw::rows_n(M) : 32;
+}
+
+static SwPlan make_sw_plan(int n_tok, int n_head, int hd, int n_kv, int num_sms, const fr_attn_opts& o,
+                           size_t ws_bytes) {
     SwPlan p;
+    const int M = n_tok * n_head;
+    p.nq = sw_slice_rows(n_tok, n_head, hd, n_kv, o);
+    p.slices = (M + p.nq - 1) / p.nq;
+    num_sms = max(1, num_sms / p.slices);                 // one CTA per SM: KV splits per slice
+    const int force_splits = o.force_splits;
     const int units = (n_kv + 15) / 16;
     int S = force_splits > 0 ? force_splits : num_sms;
     S = max(1, min(S, min(units, min(num_sms, tc::kMaxMergeSplits))));
@@ -589,6 +622,7 @@ static fr_status decode_attn_impl(const uint16_t* q16, const float* q, int64_t q
     if (opts) o = *opts;
     if (o.engine < 0 || o.engine > 1 || o.force_splits < 0 || o.wait_probe_iters < 0) return FR_ERR_INVALID_ARG;
     if (o.merge_mode < 0 || o.merge_mode > 2 || o.layout < 0 || o.layout > 2) return FR_ERR_INVALID_ARG;
+    if (o.slice_rows != 0 && o.slice_rows != 16 && o.slice_rows != 32 && o.slice_rows != 64) return FR_ERR_INVALID_ARG;
     if (o.layout == 2 && (o.engine != 0 || !sw_shape_ok(n_tok, n_head, hd))) return FR_ERR_UNSUPPORTED;
     if (o.force_cluster != 0 && o.force_cluster != 1 && o.force_cluster != 2 && o.force_cluster != 4 &&
         o.force_cluster != 8)
@@ -627,7 +661,7 @@ static fr_status decode_attn_impl(const uint16_t* q16, const float* q, int64_t q
     unsigned char* w = static_cast<unsigned char*>(ws);
 
     if (pick_layout(n_tok, n_head, hd, n_kv, o) == 2) {
-        const SwPlan p = make_sw_plan(M, hd, n_kv, sms, o.force_splits, ws_bytes);
+        const SwPlan p = make_sw_plan(n_tok, n_head, hd, n_kv, sms, o, ws_bytes);
         sw::SwLaunch L;
         memset(&L, 0, sizeof(L));
         sw::SwArgs& a = L.args;
@@ -667,7 +701,8 @@ static fr_status decode_attn_impl(const uint16_t* q16, const float* q, int64_t q
         L.k_rs = k_rs;
         L.v_rs = v_rs;
         L.m_rs = m_rs;
-        return sw::launch_sw(L, hd, stream);     // the split merge happens inside the launch
+        a.slices = p.slices;
+        return sw::launch_sw(L, hd, p.nq, stream);     // the split merge happens inside the launch
     }
 
     if (o.engine == 0) {
@@ -788,7 +823,8 @@ extern "C" fr_status fr_decode_attn_plan(int n_tok, int n_head, int hd, int n_kv
     memset(&o, 0, sizeof(o));
     if (opts) o = *opts;
     if (o.engine < 0 || o.engine > 1 || o.force_splits < 0 || o.merge_mode < 0 || o.merge_mode > 2 ||
-        o.layout < 0 || o.layout > 2)
+        o.layout < 0 || o.layout > 2 ||
+        (o.slice_rows != 0 && o.slice_rows != 16 && o.slice_rows != 32 && o.slice_rows != 64))
         return FR_ERR_INVALID_ARG;
     if (o.layout == 2 && (o.engine != 0 || !sw_shape_ok(n_tok, n_head, hd))) return FR_ERR_UNSUPPORTED;
     if (o.force_cluster != 0 && o.force_cluster != 1 && o.force_cluster != 2 && o.force_cluster != 4 &&
@@ -802,14 +838,16 @@ extern "C" fr_status fr_decode_attn_plan(int n_tok, int n_head, int hd, int n_kv
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return FR_ERR_CUDA;
     memset(plan, 0, sizeof(*plan));
     plan->engine = o.engine;
+    plan->row_slices = 1;
     plan->layout = pick_layout(n_tok, n_head, hd, n_kv, o);
     if (plan->layout == 2) {
-        const SwPlan p = make_sw_plan(M, hd, n_kv, sms, o.force_splits, workspace_bytes);
+        const SwPlan p = make_sw_plan(n_tok, n_head, hd, n_kv, sms, o, workspace_bytes);
         plan->row_tiles = 1;
         plan->splits = p.splits;
         plan->cluster = 1;
         plan->merge_kernel = 0;              // merged inside the launch
         plan->keys_on_m = 1;
+        plan->row_slices = p.slices;
     } else if (o.engine == 0) {
         bool ok = true;
         const TcPlan p = choose_tc_plan(M, hd, n_kv, sms, o, workspace_bytes, &ok);

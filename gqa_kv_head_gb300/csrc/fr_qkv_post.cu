@@ -319,7 +319,7 @@ extern "C" const char* fr_status_string(fr_status s) {
     return "unknown fr_status";
 }
 
-extern "C" int fr_abi_version(void) { return (3 << 16) | 0; }
+extern "C" int fr_abi_version(void) { return (4 << 16) | 0; }
 
 extern "C" fr_status fr_qkv_post(const float* q, int64_t q_tok_stride, const int32_t* pos,
                                  int n_tok, int n_head, int hd, const fr_rope_params* rp,

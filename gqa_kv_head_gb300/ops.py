@@ -136,10 +136,11 @@ def _row_stride(t, name):
 
 def decode_attn(k, v, n_tok, n_head, *, q16=None, q=None, pos=None, rope=None, q_scale=None,
                 mask=None, kq_scale=1.0, out=None, workspace=None, splits=None, cluster=None,
-                engine=None, wait_probe_iters=0, merge_mode=None, layout=None, stream=None):
+                engine=None, wait_probe_iters=0, merge_mode=None, layout=None, slice_rows=None, stream=None):
     """fr_decode_attn (fused qkv_post when q16 is None). Returns out
-    [n_tok, n_head, hd] f32. splits / cluster / engine / wait_probe_iters go
-    through the fr_decode_attn_ex test hook."""
+    [n_tok, n_head, hd] f32. splits / cluster / engine / wait_probe_iters /
+    merge_mode / layout / slice_rows go through the fr_decode_attn_ex test
+    hook."""
     lib = _abi.load()
     _check_dev(k, v, q16, q, pos, mask, out, workspace)
     n_kv, hd = k.shape[0], k.shape[1]
@@ -162,27 +163,28 @@ def decode_attn(k, v, n_tok, n_head, *, q16=None, q=None, pos=None, rope=None, q
             _ptr(mask), 0 if mask is None else _row_stride(mask, "mask"), n_tok, n_head, hd, n_kv,
             float(kq_scale), _ptr(out), _ptr(workspace), workspace.numel()]
     if (splits is None and cluster is None and engine is None and not wait_probe_iters and not merge_mode
-            and not layout):
+            and not layout and not slice_rows):
         st = lib.fr_decode_attn(*args, _stream(stream))
         _abi.check(st, "fr_decode_attn")
     else:
         opts = FrAttnOpts(int(engine or 0), int(splits or 0), int(cluster or 0), int(wait_probe_iters),
-                          int(merge_mode or 0), int(layout or 0))
+                          int(merge_mode or 0), int(layout or 0), int(slice_rows or 0))
         st = lib.fr_decode_attn_ex(*args, ctypes.byref(opts), _stream(stream))
         _abi.check(st, "fr_decode_attn_ex")
     return out
 
 
 def decode_attn_plan(n_tok, n_head, hd, n_kv, *, fused_qkv_post=True, workspace_bytes=None,
-                     splits=None, cluster=None, engine=None, merge_mode=None, layout=None):
+                     splits=None, cluster=None, engine=None, merge_mode=None, layout=None, slice_rows=None):
     """fr_decode_attn_plan: the launch shape a call with these arguments would
     use on the current device (nothing is launched). Returns a dict with
-    engine, row_tiles, splits, cluster, merge_kernel, launches, keys_on_m, layout."""
+    engine, row_tiles, splits, cluster, merge_kernel, launches, keys_on_m,
+    layout, row_slices."""
     lib = _abi.load()
     if workspace_bytes is None:
         workspace_bytes = workspace_size(n_tok, n_head, hd, n_kv)
     opts = FrAttnOpts(int(engine or 0), int(splits or 0), int(cluster or 0), 0, int(merge_mode or 0),
-                      int(layout or 0))
+                      int(layout or 0), int(slice_rows or 0))
     plan = _abi.FrAttnPlan()
     st = lib.fr_decode_attn_plan(n_tok, n_head, hd, n_kv, 1 if fused_qkv_post else 0, int(workspace_bytes),
                                  ctypes.byref(opts), ctypes.byref(plan))

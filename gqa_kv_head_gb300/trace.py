@@ -1,7 +1,7 @@
 """Timeline of the keys-on-M attention kernel (attn_sw_kernel), from the
 global-timer stamps of its FR_TRACE build.
 
-    python -m gqa_kv_head_gb300.trace sweep:256:1:65536 [more workloads ...]
+    python -m gqa_kv_head_gb300.trace [--slice-rows 16|32|64] sweep:256:1:65536 [more workloads ...]
 
 Builds the instrumented variant of the library into _build_trace/ (the
 library itself has no stamps), runs fused calls of each workload on seeded
@@ -28,23 +28,29 @@ def main(argv):
     import gen
 
     layout = 2
+    slice_rows = None
+    if argv and argv[0] == "--slice-rows":
+        slice_rows = int(argv[1])
+        argv = argv[2:]
     for name in argv:
         w = gen.make_workload(name)
-        plan = ops.decode_attn_plan(w.n_tok, w.n_head, w.hd, w.n_kv, layout=layout,
+        plan = ops.decode_attn_plan(w.n_tok, w.n_head, w.hd, w.n_kv, layout=layout, slice_rows=slice_rows,
                                     workspace_bytes=TRACE_OFFSET)
         n_rep = max(2, math.ceil(2 * 135e6 / (4 * w.n_kv * w.hd)))
         reps = [dict(q=torch.from_numpy(w.q()).cuda(), pos=torch.from_numpy(w.pos()).cuda(),
                      k=torch.from_numpy(w.k()).cuda(), v=torch.from_numpy(w.v()).cuda(),
                      mask=None if w.mask() is None else torch.from_numpy(w.mask()).cuda())
                 for _ in range(n_rep)]
-        ws = torch.zeros(TRACE_OFFSET + plan["splits"] * SLOTS * 8, dtype=torch.uint8, device="cuda")
+        n_cta = plan["splits"] * plan["row_slices"]           # every CTA writes SLOTS stamps
+        ws = torch.zeros(TRACE_OFFSET + n_cta * SLOTS * 8, dtype=torch.uint8, device="cuda")
         out = torch.empty((w.n_tok, w.n_head, w.hd), device="cuda")
         st = torch.cuda.Stream()
 
         def call(i):
             r = reps[i % n_rep]
             ops.decode_attn(r["k"], r["v"], w.n_tok, w.n_head, q=r["q"], pos=r["pos"], rope=w.rope,
-                            mask=r["mask"], out=out, workspace=ws[:TRACE_OFFSET], stream=st, layout=layout)
+                            mask=r["mask"], out=out, workspace=ws[:TRACE_OFFSET], stream=st, layout=layout,
+                            slice_rows=slice_rows)
 
         with torch.cuda.stream(st):
             for i in range(4):
@@ -58,14 +64,15 @@ def main(argv):
             g.replay()
             g.replay()
         st.synchronize()
-        S = plan["splits"]
+        S = n_cta
         tr = ws[TRACE_OFFSET:TRACE_OFFSET + S * SLOTS * 8].view(torch.int64).view(S, SLOTS).cpu().numpy()
         smid = tr[:, 63].copy()
         tr[:, 63] = tr[:, 0]
         rel = (tr - tr[:, 0].min()) / 1000.0
         med = lambda c: float(np.median(rel[:, c]))
-        n_tiles = (w.n_kv // S + 127) // 128
-        print(f"== {name}: {S} splits, one per SM; stamps in us after the first CTA's set-up (graph replay)")
+        n_tiles = (w.n_kv // plan["splits"] + 127) // 128
+        print(f"== {name}: {plan['splits']} splits x {plan['row_slices']} row slices = {S} CTAs, one per SM; "
+              f"stamps in us after the first CTA's set-up (graph replay)")
         print(f"set-up done (median) {med(0):.2f}; launch wait over {med(4):.2f}; "
               f"Q in place {med(3):.2f} (rows landed {med(6):.2f}, roped {med(7):.2f})")
         print(f"epilogue (median): row sums {med(57):.2f}, rows stored {med(58):.2f}, fenced and arriving "

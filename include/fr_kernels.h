@@ -250,10 +250,20 @@ typedef struct fr_attn_opts {
                               FR_ERR_WORKSPACE if forced splits do not fit) */
     int layout;            /* 0 = library's choice; 1 = 128-row query tiles (the query rows
                               are the MMA's M); 2 = 128-key tiles as the MMA's M and the
-                              query rows as its N (M <= 64 rows, hd 128 or 256, n_tok <= 16:
-                              FR_ERR_UNSUPPORTED otherwise). The library's choice is 2 for
-                              M <= 32 rows and n_kv >= max(1024, 256 M) (where it measures
-                              faster), unless force_cluster or merge_mode 1 is given. */
+                              query rows as its N (M <= 128 rows, hd 128 or 256, n_tok <= 16:
+                              FR_ERR_UNSUPPORTED otherwise). The library's choice (measured
+                              faster there) is 2 with 16-row slices when n_kv >= 1024 and
+                              ceil(M/16) * n_kv <= 16384; 2 with one slice of all rows when
+                              M <= 32 and n_kv >= max(1024, 256 M); 2 with 32-row slices when
+                              hd = 128, 32 < M <= 64 and n_kv >= 16384; else 1 — unless
+                              force_cluster or merge_mode 1 is given (then 1). */
+    int slice_rows;        /* layout 2 only: 0 = library's choice; else 16, 32 or 64 query
+                              rows per CTA (the MMA's N): the M rows are cut into
+                              ceil(M / slice_rows) slices, each KV split is then read by that
+                              many CTAs (one per slice; the later reads served by L2), and
+                              the KV splits are the SMs / slices. With layout 2 forced where
+                              the library would not pick it, the default is one slice up to
+                              64 rows and 32-row slices beyond. */
 } fr_attn_opts;
 
 fr_status fr_decode_attn_ex(const uint16_t* q16,
@@ -283,6 +293,7 @@ typedef struct fr_attn_plan {
     int keys_on_m;         /* 1: 128-key tiles are the MMA's M, the query rows its N */
     int layout;            /* kernel: 1 = 128-row query tiles, 2 = keys on M (see
                               fr_attn_opts.layout) */
+    int row_slices;        /* layout 2: CTAs per KV split (slices of the query rows); else 1 */
 } fr_attn_plan;
 
 fr_status fr_decode_attn_plan(int n_tok, int n_head, int hd, int n_kv, int fused_qkv_post,

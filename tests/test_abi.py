@@ -44,7 +44,7 @@ def test_status_strings_and_version(lib):
     assert lib.fr_status_string(0) == b"FR_OK"
     for s in range(1, 6):
         assert lib.fr_status_string(s).startswith(b"FR_ERR_")
-    assert lib.fr_abi_version() >> 16 == 3
+    assert lib.fr_abi_version() >> 16 == 4
 
 
 def test_workspace_size_host_logic(lib):
@@ -91,7 +91,8 @@ def test_decode_attn_validation(lib):
     from gqa_kv_head_gb300._abi import FrAttnOpts
     ws_ok = lib.fr_decode_attn_workspace_size(4, 8, 128, 64)
     for bad in (FrAttnOpts(7, 0, 0, 0, 0), FrAttnOpts(0, -1, 0, 0, 0), FrAttnOpts(0, 0, 3, 0, 0),
-                FrAttnOpts(0, 0, 16, 0, 0), FrAttnOpts(0, 0, 0, -5, 0), FrAttnOpts(0, 0, 0, 0, 3)):
+                FrAttnOpts(0, 0, 16, 0, 0), FrAttnOpts(0, 0, 0, -5, 0), FrAttnOpts(0, 0, 0, 0, 3),
+                FrAttnOpts(0, 0, 0, 0, 0, 3), FrAttnOpts(0, 0, 0, 0, 0, 2, 24), FrAttnOpts(0, 0, 0, 0, 0, 2, -16)):
         assert lib.fr_decode_attn_ex(FAKE, None, 0, None, None, 0.0, FAKE, 128, FAKE, 128, None, 0,
                                      4, 8, 128, 64, 1.0, FAKE, FAKE, ws_ok, ctypes.byref(bad), None) == 1
 

@@ -265,10 +265,13 @@ def test_plan_reports_the_launch_shape():
     p = fr.decode_attn_plan(tiny.n_tok, tiny.n_head, tiny.hd, tiny.n_kv)
     assert p["engine"] == 0 and p["merge_kernel"] == 0 and p["launches"] == 2 and p["splits"] <= 2
     w = named_config("pi05")
-    p = fr.decode_attn_plan(w.n_tok, w.n_head, w.hd, w.n_kv)
-    assert p["merge_kernel"] == 1 and p["cluster"] == 1 and p["launches"] == 3
+    # the library's own choice here: the keys-on-M kernel, five 16-row slices, one launch
+    pa = fr.decode_attn_plan(w.n_tok, w.n_head, w.hd, w.n_kv)
+    assert pa["keys_on_m"] == 1 and pa["row_slices"] == 5 and pa["launches"] == 1 and pa["merge_kernel"] == 0
+    p = fr.decode_attn_plan(w.n_tok, w.n_head, w.hd, w.n_kv, layout=1)
+    assert p["merge_kernel"] == 1 and p["cluster"] == 1 and p["launches"] == 3 and p["row_slices"] == 1
     assert p["splits"] == 16                        # one 64-key tile per split
-    assert fr.decode_attn_plan(w.n_tok, w.n_head, w.hd, w.n_kv, fused_qkv_post=False)["launches"] == 2
+    assert fr.decode_attn_plan(w.n_tok, w.n_head, w.hd, w.n_kv, fused_qkv_post=False, layout=1)["launches"] == 2
     p1 = fr.decode_attn_plan(w.n_tok, w.n_head, w.hd, w.n_kv, merge_mode=1)
     assert p1["merge_kernel"] == 0 and p1["cluster"] > 1 and p1["launches"] == 2
     # a workspace of the in-launch size only keeps the in-launch plan, or cuts

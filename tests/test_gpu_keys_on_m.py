@@ -1,9 +1,10 @@
 """The kernel with 128-key tiles on the MMA's M side and the query rows on
-its N (layout 2: M = n_tok*n_head <= 64, hd 128 or 256), against the fp64
+its N (layout 2: M = n_tok*n_head <= 128, hd 128 or 256), against the fp64
 oracle through the C ABI: every row count up to 64 (N = 16, 32, 64 with
-padded rows), ragged KV lengths, masks, padded strides, forced split counts,
-a workspace that holds fewer split states, and the same result as the
-128-row query-tile kernel (layout 1).
+padded rows), rows cut into slices of 16, 32 or 64 (up to 128 rows, CTAs of
+one split sharing its K/V tiles), ragged KV lengths, masks, padded strides,
+forced split counts, a workspace that holds fewer split states, and the same
+result as the 128-row query-tile kernel (layout 1).
 
 FlashRT PR #185, commits "FLASH_ATTN_EXT with q_tokens <= 16 ..." and "The
 GQA query heads share the one KV head ...": one QK^T and one PV over all
@@ -27,7 +28,25 @@ def _plan(w, **kw):
     return fr.decode_attn_plan(w.n_tok, w.n_head, w.hd, w.n_kv, layout=2, **kw)
 
 
-KOM = dict(layout=2)      # the library picks this layout itself for M <= 32 rows and n_kv >= max(1024, 256 M)
+KOM = dict(layout=2)
+
+
+def _auto_rows(w):
+    """Rows per slice of the library's own keys-on-M choice (0: the 128-row
+    kernel), as include/fr_kernels.h documents it: 16-row slices for a short
+    KV range (n_kv >= 1024 and ceil(M/16)*n_kv <= 16384), one slice of all
+    rows for M <= 32 and n_kv >= max(1024, 256 M), 32-row slices for hd 128,
+    32 < M <= 64 and n_kv >= 16384."""
+    M = w.n_tok * w.n_head
+    if w.hd not in (128, 256) or w.n_tok > 16 or M > 128:
+        return 0
+    if w.n_kv >= 1024 and -(-M // 16) * w.n_kv <= 16384:
+        return 16
+    if M <= 32 and w.n_kv >= max(1024, 256 * M):
+        return 16 if M <= 16 else 32
+    if w.hd == 128 and 32 < M <= 64 and w.n_kv >= 16384:
+        return 32
+    return 0
 
 
 @pytest.mark.parametrize("hd", [128, 256])
@@ -38,8 +57,10 @@ def test_row_counts(hd, n_tok, n_head):
                  rope=RopeParams(n_dims=hd, freq_base=10000.0), positions=tuple(range(2999 - n_tok + 1, 3000)),
                  mask_kind="causal", seed=n_tok * 7 + n_head)
     assert _plan(w)["keys_on_m"] == 1
-    auto = fr.decode_attn_plan(w.n_tok, w.n_head, w.hd, w.n_kv)["keys_on_m"]
-    assert auto == (1 if w.M <= 32 and w.n_kv >= max(1024, 256 * w.M) else 0)
+    auto = fr.decode_attn_plan(w.n_tok, w.n_head, w.hd, w.n_kv)
+    rows = _auto_rows(w)
+    assert auto["keys_on_m"] == (1 if rows else 0)
+    assert auto["row_slices"] == (-(-w.M // rows) if rows else 1)
     d = to_device(w)
     out = _rows(run_fused(w, d, **KOM))
     ref = oracle_out(w)
@@ -135,11 +156,55 @@ def test_fully_masked_token_is_zero():
 
 
 def test_layout_option_validation():
-    w = named_config("c3")                      # 128 rows: no keys-on-M plan
+    w = Workload("wide", n_head=9, n_tok=16, hd=256, n_kv=512, rope=RopeParams(n_dims=256),
+                 positions=tuple(range(496, 512)), mask_kind="causal")      # 144 rows: no keys-on-M plan
     d = to_device(w)
     with pytest.raises(fr.FrError) as e:
         run_fused(w, d, layout=2)
     assert e.value.status == 2
+    with pytest.raises(fr.FrError) as e:                                     # not 16, 32 or 64 rows per slice
+        run_fused(named_config("c3"), to_device(named_config("c3")), layout=2, slice_rows=48)
+    assert e.value.status == 1
     t = named_config("tiny")                    # hd 64
     with pytest.raises(fr.FrError):
         run_fused(t, to_device(t), layout=2)
+
+
+@pytest.mark.parametrize("hd", [128, 256])
+@pytest.mark.parametrize("slice_rows", [16, 32, 64])
+@pytest.mark.parametrize("n_tok,n_head", [(16, 8), (8, 8), (4, 8), (3, 5), (9, 11), (2, 64), (13, 7), (1, 20)])
+def test_row_slices(hd, slice_rows, n_tok, n_head):
+    """The query rows cut into slices of slice_rows (the MMA's N): one CTA per
+    (KV split, slice), each roping or loading only its own rows (slices may
+    cut through a token's heads), the merge over every slice's rows."""
+    w = Workload("slices", n_head=n_head, n_tok=n_tok, hd=hd, n_kv=5000,
+                 rope=RopeParams(n_dims=hd, freq_base=10000.0), positions=tuple(range(4999 - n_tok + 1, 5000)),
+                 mask_kind="random5", seed=n_tok * 13 + n_head + slice_rows)
+    p = _plan(w, slice_rows=slice_rows)
+    assert p["keys_on_m"] == 1 and p["row_slices"] == (w.M + slice_rows - 1) // slice_rows
+    d = to_device(w, k_pad=8, q_extra_heads=1)
+    ref = oracle_out(w)
+    fused = run_fused(w, d, slice_rows=slice_rows, **KOM)
+    assert_close(_rows(fused), ref, f"{n_tok}x{n_head} hd {hd} / {slice_rows}")
+    two_call, _ = run_two_call(w, d, slice_rows=slice_rows, **KOM)
+    torch.cuda.synchronize()
+    assert torch.equal(fused, two_call)          # the kernel's own RoPE gives qkv_post's bits
+
+
+@pytest.mark.parametrize("name", ["sweep:256:16:65536", "sweep:128:16:4096", "sweep:256:8:1024"])
+@pytest.mark.parametrize("splits", [1, 3, 1000])
+def test_row_slices_forced_splits(name, splits):
+    w = make_workload(name)
+    d = to_device(w)
+    p = _plan(w, splits=splits, slice_rows=32)
+    assert p["row_slices"] == (w.M + 31) // 32 and p["splits"] <= max(1, splits)
+    assert_close(_rows(run_fused(w, d, splits=splits, slice_rows=32, **KOM)), oracle_out(w), f"{name} splits={splits}")
+
+
+@pytest.mark.parametrize("n_kv", [1, 129, 20037])
+def test_row_slices_ragged_kv(n_kv):
+    w = Workload(f"slices-ragged{n_kv}", n_head=8, n_tok=16, hd=256, n_kv=n_kv,
+                 rope=RopeParams(n_dims=256, freq_base=10000.0), positions=tuple(range(n_kv - 1, n_kv + 15)),
+                 mask_kind="causal", seed=n_kv % 31)
+    d = to_device(w, k_pad=16, mask_pad=8)
+    assert_close(_rows(run_fused(w, d, slice_rows=32, **KOM)), oracle_out(w), w.name)
