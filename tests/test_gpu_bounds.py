@@ -2,8 +2,8 @@
 every output buffer the library writes (out, the workspace, q16_out, the KV
 cache) sits between two 4 KiB margins filled with a byte pattern; after a call
 the margins must be byte-identical. Covers the named workloads, ragged row and
-key counts, both split-merge strategies, forced clusters and split counts,
-prefill windows and fr_kv_append. Also: pointers that are not memory of the
+key counts, both split-merge strategies, forced clusters and split counts, the
+keys-on-M kernel's row slices, prefill windows and fr_kv_append. Also: pointers that are not memory of the
 current GPU are rejected on the host before any launch."""
 import ctypes
 
@@ -65,6 +65,21 @@ def test_guards_named_and_sweep(name):
     d = to_device(w)
     out = _guarded_call(w, d)
     assert_close(_rows(out), oracle_out(w), name)
+
+
+@pytest.mark.parametrize("hd", [128, 256])
+@pytest.mark.parametrize("opts", [{"slice_rows": 16}, {"slice_rows": 32}, {"slice_rows": 64},
+                                  {"slice_rows": 16, "splits": 1}, {"slice_rows": 32, "splits": 1000}])
+def test_guards_keys_on_m_slices(hd, opts):
+    """The keys-on-M kernel with ragged rows cut into slices (M = 35: slices
+    end inside a token's heads and the last one is short), a one-key last
+    tile, padded strides, one split (each slice normalises its own rows) and
+    many."""
+    w = Workload("ragged-slices", n_head=5, n_tok=7, hd=hd, n_kv=4097, rope=RopeParams(n_dims=hd),
+                 positions=tuple(range(4090, 4097)), mask_kind="random5", seed=13)
+    d = to_device(w, k_pad=16, mask_pad=8, q_extra_heads=2)
+    out = _guarded_call(w, d, layout=2, **opts)
+    assert_close(_rows(out), oracle_out(w), f"ragged slices hd {hd} {opts}")
 
 
 @pytest.mark.parametrize("hd", [64, 128, 256])
