@@ -208,3 +208,38 @@ def test_row_slices_ragged_kv(n_kv):
                  mask_kind="causal", seed=n_kv % 31)
     d = to_device(w, k_pad=16, mask_pad=8)
     assert_close(_rows(run_fused(w, d, slice_rows=32, **KOM)), oracle_out(w), w.name)
+
+
+def test_barrier_words_across_grid_sizes():
+    """The grid barrier's words in one workspace return to zero after every
+    call, so calls with different grids (40 sliced CTAs, 152 CTAs, one split
+    without a barrier, a timed-out probe) can follow each other on it in any
+    order, captured in a graph too."""
+    shapes = [make_workload("pi05"), make_workload("sweep:256:1:65536"), make_workload("sweep:128:4:4096"),
+              make_workload("sweep:256:16:2048")]
+    devs = [to_device(w) for w in shapes]
+    refs = [oracle_out(w) for w in shapes]
+    nbytes = max(fr.workspace_size(w.n_tok, w.n_head, w.hd, w.n_kv) for w in shapes)
+    ws = torch.zeros(nbytes, dtype=torch.uint8, device="cuda")
+    order = [0, 1, 2, 3, 1, 0, 3, 2, 0]
+    for i in order:
+        w, d = shapes[i], devs[i]
+        assert_close(_rows(run_fused(w, d, workspace=ws, **KOM)), refs[i], f"{w.name} in sequence")
+        assert_close(_rows(run_fused(w, d, workspace=ws, splits=1, **KOM)), refs[i], f"{w.name} one split")
+    fr.workspace_check(ws)
+    # graph of mixed calls on the same workspace
+    outs = [torch.empty((w.n_tok, w.n_head, w.hd), dtype=torch.float32, device="cuda") for w in shapes]
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        for i in order:
+            run_fused(shapes[i], devs[i], workspace=ws, out=outs[i], stream=s, **KOM)
+    for o in outs:
+        o.zero_()
+    g.replay()
+    g.replay()
+    torch.cuda.synchronize()
+    for i, w in enumerate(shapes):
+        assert_close(_rows(outs[i]), refs[i], f"{w.name} replayed")
+    fr.workspace_check(ws)
