@@ -101,13 +101,41 @@ def roofline_entry(w, attn_us, attn_bytes, peaks, traffic, traffic_source, kerne
                  "frac": gbs / peaks["hbm_gbs"], "peak_kind": f"{peaks['kind']} hbm_gbs (burst copy)"}, **base)
 
 
+def _strip_comments(src):
+    """C/C++ source without its // and /* */ comments (string and character
+    literals kept), so that comment edits leave the kernel hash unchanged."""
+    out, i, n = [], 0, len(src)
+    while i < n:
+        c = src[i]
+        if c in "\"'":
+            j = i + 1
+            while j < n and src[j] != c:
+                j += 2 if src[j] == "\\" else 1
+            out.append(src[i:j + 1])
+            i = j + 1
+        elif src.startswith("//", i):
+            j = src.find("\n", i)
+            i = n if j < 0 else j
+        elif src.startswith("/*", i):
+            j = src.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+        else:
+            out.append(c)
+            i += 1
+    return "".join(out)
+
+
 def kernel_source_hash():
+    """Hash of the kernel sources' code (comments excluded, whitespace runs as
+    one space): the traffic figures of a committed ncu summary hold while it
+    is unchanged."""
     import hashlib
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "gqa_kv_head_gb300", "csrc")
     for fn in sorted(os.listdir(csrc)):
         if fn.endswith((".cu", ".cuh")):
-            h.update(open(os.path.join(csrc, fn), "rb").read())
+            code = _strip_comments(open(os.path.join(csrc, fn), encoding="utf-8").read())
+            h.update(" ".join(code.split()).encode())          # whitespace runs as one space
     return h.hexdigest()[:16]
 
 

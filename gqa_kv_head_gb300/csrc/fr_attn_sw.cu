@@ -5,20 +5,18 @@
 // padded f16 KV head ..." (QK^T with the K operand shared by every GQA head,
 // masked fp32-accurate softmax, PV into [hd, n_head, n_tok]) and "The GQA query
 // heads share the one KV head, so the per-head batched QK^T and PV GEMMs
-// collapse into single GEMMs over all n_head*n_tok query rows". With M =
-// n_tok*n_head <= 64 rows, a 128-row query tile (the MMA's M) would be mostly
-// padding; here 128 keys are the MMA's M and the query rows its N (16, 32 or
-// 64), so the tensor work follows the real rows.
+// collapse into single GEMMs over all n_head*n_tok query rows". For decode
+// shapes a 128-row query tile (the MMA's M) would be mostly padding; here 128
+// keys are the MMA's M and a slice of NQ query rows its N (16, 32 or 64), so
+// the tensor work follows the real rows.
 //
-// One CTA = one KV split x one slice of NQ query rows (one CTA per SM; with
-// more than 64 rows, or when the plan asks for it, the rows are cut into
-// slices whose CTAs read the same K/V tiles, the later reads served by L2);
-// W softmax warps (8 for 16 rows,
-// 16 for 32 or 64 rows) and two more:
+// One CTA = one KV split x one slice of NQ of the M <= 128 query rows (one CTA
+// per SM; when M is cut into several slices, the slices' CTAs of a split read
+// the same K/V tiles, the later reads served by L2); W softmax warps (8 for 16
+// rows, 16 for 32 or 64 rows) and two more:
 //   warps 0..W-1  softmax, one thread per (key of the tile, W/4-th of the
-//              query rows): warps w, w + 4, ... share TMEM lane quadrant w % 4
-//              (keys 32(w%4)..+31 of S^T), each owning a slice of at most 16
-//              rows.
+//              slice's rows): warps w, w + 4, ... share TMEM lane quadrant
+//              w % 4 (keys 32(w%4)..+31 of S^T), each owning at most 16 rows.
 //              kq_scale and the mask; the per-row reference maxima are only
 //              recomputed when some score exceeds its row's reference by more
 //              than 2^8 (one barrier-OR vote per tile; the row maxima then come
@@ -31,19 +29,20 @@
 //   warp W     TMA producer: one ring of 32 KiB stages (128 keys x 128 dims of
 //              K or of V, two 64-dim boxes) filled in exactly the order the
 //              MMAs consume them, a ring of mask tiles, and in the fused call
-//              the f32 Q rows (one bulk copy per token) for the in-kernel RoPE.
+//              the slice's f32 Q rows (one bulk copy per token) for the
+//              in-kernel RoPE.
 //   warp W+1   MMA issuer: S^T_j = K_j Q^T (A = K stage, K-major; B = the Q
 //              rows), O^T += V_j^T [P_hi; P_lo]^T (A = V stage and B = P^T, both
 //              read MN-major; the P_lo product accumulates in its own columns).
 //              S_{j+1} is issued before PV_j, so the softmax of tile j+1
 //              overlaps PV_j.
-// In the fused call the kernel ropes the Q rows itself with qkv_post's
+// In the fused call the kernel ropes its rows itself with qkv_post's
 // arithmetic (fr_qkv_post's device routines), so one call is one launch.
 // Each split writes its unnormalised O rows with its row maxima (log2 units)
-// and sums to the workspace (part_o[s][r][hd]: a split's rows are contiguous);
-// after a bounded grid barrier (cooperative launch) the softmax warps of every
-// CTA merge a share of the output rows. A single split normalises and writes
-// the output rows itself.
+// and sums to the workspace (part_o[s][r][hd] over all M rows: a split's rows
+// are contiguous); after a bounded grid barrier (cooperative launch) the
+// softmax warps of every CTA merge a share of the output rows. A single split
+// normalises and writes the output rows itself.
 // Every mbarrier wait is bounded; a wait that gives up sets the status word,
 // and the CTA still drains its copies and MMAs and frees its TMEM.
 #include <math.h>
