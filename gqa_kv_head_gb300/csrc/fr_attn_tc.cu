@@ -20,8 +20,9 @@
 //              is large.
 //   warp 8     TMA producer: one thread fills separate rings of K, V and
 //              mask tiles, refilling whichever slot frees first (a K slot is
-//              free again once S_j is computed, so K runs ahead of V); the
-//              first tiles are requested before the Q prologue.
+//              free again once S_j is computed, so K runs ahead of V); it
+//              also loads the Q tile, after the first K tile and before the
+//              rest of the first ring fill.
 //   warp 9     MMA issuer: S_j = Q K_j^T (SS form, S double-buffered in TMEM),
 //              O += P_hi,j V_j + P_lo,j V_j (A operand from TMEM, V read
 //              MN-major), commits.
@@ -249,8 +250,6 @@ attn_tc_kernel(const __grid_constant__ TcArgs a, const __grid_constant__ Maps mp
     // could hold SMs that later CTAs of this grid need.
     if (a.early_dep) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
-    // K/V/mask tiles need no Q: the first ones are requested before the
-    // prologue.
     // mask rows: all tokens when n_tok <= kMaskWin, else the kMaskWin tokens
     // from this row tile's first one (they hold every token of the tile)
     const int mask_rows = min(a.n_tok, kMaskWin);
@@ -278,25 +277,30 @@ attn_tc_kernel(const __grid_constant__ TcArgs a, const __grid_constant__ Maps mp
             tma_load_2d(smem_addr(sMask(st) + mb * C::MASK_BOX), &mp.mask, (t0 + i) * BN + mb * 64, mask_t0,
                         bar(C::B_MFULL + st));
     };
-    // one producer thread feeds all three rings: first the slots every ring
-    // starts with, tile by tile
+    // ---- prologue: one producer thread requests the first K tile (and its
+    // mask tile), then the 128 Q rows as f16 (SW128 K-major, every CTA of a
+    // cluster loads the whole tile itself: the rows are in L2, qkv_post has
+    // just written them), then the rest of the slots every ring starts with.
+    // When the rows come from the qkv_post grid launched just before this one
+    // (programmatic dependent launch), the wait for that grid sits between
+    // the first K tile and the Q rows: the K tile overlaps it, and the Q rows
+    // are not queued behind the whole first ring fill (requesting that ring
+    // before the wait put the rows in place ~2 us after it ended, and the
+    // whole call 0.1-0.5 us slower; requesting no tile before it, or both
+    // first K tiles, was slower too).
     if (warp == kProdWarp && lane == 0) {
-        for (int i = 0; i < max(C::KS, max(C::VS, C::MS)) && i < n_my; ++i) {
-            if (i < C::KS) load_k(i);
-            if (a.has_mask && i < C::MS) load_m(i);
-            if (i < C::VS) load_v(i);
+        if (n_my > 0) {
+            load_k(0);
+            if (a.has_mask) load_m(0);
         }
-    }
-
-    // ---- prologue: the 128 Q rows as f16, SW128 K-major in every CTA --------
-    // Every CTA of a cluster loads the whole tile itself (the rows are in L2:
-    // qkv_post has just written them). When the rows come from the qkv_post
-    // grid launched just before this one (programmatic dependent launch), wait
-    // for that grid here: everything above overlapped it.
-    if (tid == 0) {
         asm volatile("griddepcontrol.wait;" ::: "memory");
         for (int b = 0; b < C::NB; ++b)
             tma_load_2d(smem_addr(sQ + b * C::Q_BOX), &mp.q16, b * 64, row0, bar(C::B_QFULL));
+        for (int i = 0; i < max(C::KS, max(C::VS, C::MS)) && i < n_my; ++i) {
+            if (i > 0 && i < C::KS) load_k(i);
+            if (a.has_mask && i > 0 && i < C::MS) load_m(i);
+            if (i < C::VS) load_v(i);
+        }
     }
 
     if (a.probe_iters && tid == 0) {
