@@ -54,9 +54,10 @@ bool encode_f16_2d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t ro
                    uint32_t box_inner, uint32_t box_rows, bool swizzle128);
 fr_status launch_tc(const TcLaunch& L, int hd, cudaStream_t stream);
 // Merge of the split states written in merge-kernel mode (programmatic
-// dependent launch after the attention grid).
+// dependent launch after the attention grid). ws = the workspace start, where
+// the FR_TRACE build stamps its timeline (unused otherwise).
 fr_status launch_merge(const float* part_o, const float2* part_ml, float* out, int M, int splits, int hd,
-                       int rstride, cudaStream_t stream);
+                       int rstride, unsigned* ws, cudaStream_t stream);
 
 }  // namespace tc
 

@@ -53,6 +53,7 @@
 #include "fr_attn.h"
 #include "fr_common.cuh"
 #include "fr_sm100.cuh"
+#include "fr_trace.cuh"
 
 namespace fr {
 namespace tc {
@@ -244,6 +245,10 @@ attn_tc_kernel(const __grid_constant__ TcArgs a, const __grid_constant__ Maps mp
     else __syncthreads();               //     (one-CTA cluster: a CTA barrier is enough)
     tc_fence_after();
     const uint32_t tbase = *sTmemBase;
+    if (tid == 0) {
+        FR_STAMP(0);                             // set-up done
+        FR_STAMP_SMID();
+    }
     // a dependent grid (the merge kernel, or the next call's qkv_post) may be
     // scheduled now; it waits for this grid's completion before reading what it
     // writes. Only when this grid is one wave: otherwise waiting dependent CTAs
@@ -294,6 +299,7 @@ attn_tc_kernel(const __grid_constant__ TcArgs a, const __grid_constant__ Maps mp
             if (a.has_mask) load_m(0);
         }
         asm volatile("griddepcontrol.wait;" ::: "memory");
+        FR_STAMP(4);                                 // the grids ahead are complete
         for (int b = 0; b < C::NB; ++b)
             tma_load_2d(smem_addr(sQ + b * C::Q_BOX), &mp.q16, b * 64, row0, bar(C::B_QFULL));
         for (int i = 0; i < max(C::KS, max(C::VS, C::MS)) && i < n_my; ++i) {
@@ -360,6 +366,7 @@ attn_tc_kernel(const __grid_constant__ TcArgs a, const __grid_constant__ Maps mp
             // the Q tile must have landed (full limit: the copy writes this
             // CTA's shared memory)
             if (!mbar_wait(bar(C::B_QFULL), 0, limit)) record_timeout(a.status, 1u);
+            FR_STAMP(3);                             // the Q tile is in place
             tc_fence_after();
             constexpr uint32_t idS = idesc_f16_f32(kRows, BN, 0, 0);
             constexpr uint32_t idO = idesc_f16_f32(kRows, HD, 0, 1);
@@ -367,6 +374,7 @@ attn_tc_kernel(const __grid_constant__ TcArgs a, const __grid_constant__ Maps mp
             auto issue_s = [&](int i) {
                 const int st = i % C::KS;
                 wait(bar(C::B_KFULL + st), (i / C::KS) & 1);
+                if (i < 8) FR_STAMP(36 + i);             // K_i has landed
                 tc_fence_after();
                 const uint32_t k_base = smem_addr(sK(st));
                 const uint32_t d = tbase + C::TM_S + (i & 1) * BN;
@@ -378,6 +386,7 @@ attn_tc_kernel(const __grid_constant__ TcArgs a, const __grid_constant__ Maps mp
                 }
                 mma_commit(bar(C::B_SFULL + (i & 1)));
                 mma_commit(bar(C::B_KEMPTY + st));
+                if (i < 7) FR_STAMP(8 + 4 * i + 2);      // S_i issued
             };
             // S_{i+1} is issued ahead of PV_i, waiting for its K tile if need be, so
             // the softmax of tile i+1 can start as soon as that of tile i ends. No
@@ -390,6 +399,7 @@ attn_tc_kernel(const __grid_constant__ TcArgs a, const __grid_constant__ Maps mp
                 if (s_next == i + 1 && s_next < n_my) issue_s(s_next++);
                 wait(bar(C::B_PFULL + (i & 1)), (i >> 1) & 1);
                 wait(bar(C::B_VFULL + i % C::VS), (i / C::VS) & 1);
+                if (i < 8) FR_STAMP(44 + i);             // P_i written and V_i landed
                 tc_fence_after();
                 const uint32_t v_base = smem_addr(sV(i % C::VS));
 #pragma unroll
@@ -404,6 +414,7 @@ attn_tc_kernel(const __grid_constant__ TcArgs a, const __grid_constant__ Maps mp
                 }
                 mma_commit(bar(C::B_ODONE));
                 mma_commit(bar(C::B_VEMPTY + i % C::VS));
+                if (i < 7) FR_STAMP(8 + 4 * i + 3);      // PV_i issued
             }
             // drain: no MMA may still be running when TMEM is freed
             mma_commit(bar(C::B_MMADONE));
@@ -418,6 +429,7 @@ attn_tc_kernel(const __grid_constant__ TcArgs a, const __grid_constant__ Maps mp
         const int c_base = half * HB;
         for (int i = 0; i < n_my; ++i) {
             wait(bar(C::B_SFULL + (i & 1)), (i >> 1) & 1);
+            if (tid == 0 && i < 7) FR_STAMP(8 + 4 * i);          // softmax of tile i starts
             tc_fence_after();
             float x[HB];
             float pm = -INFINITY;
@@ -509,11 +521,13 @@ attn_tc_kernel(const __grid_constant__ TcArgs a, const __grid_constant__ Maps mp
                 tmem_wait_st();
             }
             m_ref = m_new;
+            if (tid == 0 && i < 7) FR_STAMP(8 + 4 * i + 1);      // P_i written
             tc_fence_before();
             mbar_arrive(bar(C::B_PFULL + (i & 1)));
         }
         if (n_my > 0) {
             if (!mbar_wait(bar(C::B_ODONE), (n_my - 1) & 1, limit)) record_timeout(a.status, 1u);
+            if (tid == 0) FR_STAMP(1);           // every MMA complete
             tc_fence_after();
         }
         // the row sum is the sum of both halves' partial sums
@@ -522,6 +536,7 @@ attn_tc_kernel(const __grid_constant__ TcArgs a, const __grid_constant__ Maps mp
         l_part += sLX[(half ^ 1) * kRows + r];
     }
     __syncthreads();                    // every async load drained, every MMA done
+    if (tid == 0) FR_STAMP(57);
     tc_fence_before();
     if (CS > 1) cluster_sync();         // #3: every CTA is done with its data region
 
@@ -562,6 +577,7 @@ attn_tc_kernel(const __grid_constant__ TcArgs a, const __grid_constant__ Maps mp
                 a.part_ml[(int64_t)(rt * a.splits + split) * kRows + r] =
                     n_my > 0 ? make_float2(m_ref, l_part) : make_float2(-INFINITY, 0.f);
             if (lane == 0) bulk_wait_all();     // performed before the grid completes
+            if (tid == 0) FR_STAMP(58);          // this split's state is stored
         }
     } else {
     // ---- push (m, l, O) rows to the CTA that owns them in this cluster ------
@@ -730,6 +746,7 @@ attn_tc_kernel(const __grid_constant__ TcArgs a, const __grid_constant__ Maps mp
     // ---- teardown --------------------------------------------------------------
     tc_fence_before();
     __syncthreads();
+    if (tid == 0) FR_STAMP(2);                   // done
     if (warp == kMmaWarp) {
         __syncwarp();
         tc_fence_after();
@@ -752,10 +769,17 @@ attn_tc_kernel(const __grid_constant__ TcArgs a, const __grid_constant__ Maps mp
 constexpr int kMergeWarps = 32;
 constexpr int kMergeSplitsPerWarp = 6;          // nw = ceil(splits / 6) warps per unit
 
+// The FR_TRACE build holds the untraced kernel's register count (two CTAs of
+// up to 1024 threads per SM), so that its stamps do not change the occupancy.
+#ifdef FR_TRACE
+#define FR_MERGE_BOUNDS __launch_bounds__(kMergeWarps * 32, 2)
+#else
+#define FR_MERGE_BOUNDS __launch_bounds__(kMergeWarps * 32)
+#endif
 template <int HD>
-__global__ void __launch_bounds__(kMergeWarps * 32)
+__global__ void FR_MERGE_BOUNDS
 attn_merge_kernel(const float* __restrict__ part_o, const float2* __restrict__ part_ml, float* __restrict__ out,
-                  int M, int splits, int nw, int early, int rstride) {
+                  int M, int splits, int nw, int early, int rstride, unsigned* trace_ws) {
     constexpr int CWM = HD < 128 ? HD : 128;
     constexpr int NCH = HD / CWM;
     constexpr int LANES = CWM / 4;
@@ -772,7 +796,12 @@ attn_merge_kernel(const float* __restrict__ part_o, const float2* __restrict__ p
     const bool live = uw < upc && unit < M * NCH;
     const int row = live ? unit / NCH : 0, chunk = live ? unit - (unit / NCH) * NCH : 0;
     const int rt = row / rstride, rr = row - rt * rstride;
+    if (tid == 0) {
+        FR_STAMP_AT(trace_ws, 0);                           // resident
+        FR_STAMP_SMID_AT(trace_ws);
+    }
     asm volatile("griddepcontrol.wait;" ::: "memory");     // the attention grid is complete
+    if (tid == 0) FR_STAMP_AT(trace_ws, 1);
     // A dependent launch (the next call's qkv_post) may start now only when this
     // grid fits in one wave; otherwise its waiting CTAs would hold the SMs the
     // later merge CTAs need.
@@ -829,6 +858,10 @@ attn_merge_kernel(const float* __restrict__ part_o, const float2* __restrict__ p
             out[(int64_t)row * HD + chunk * CWM + c] = L > 0.f ? sum / L : 0.f;
         }
     }
+#ifdef FR_TRACE
+    __syncthreads();
+    if (tid == 0) FR_STAMP_AT(trace_ws, 2);                 // done
+#endif
 }
 
 // The same merge for a few splits (<= kSmallMergeSplits): one warp per unit,
@@ -888,7 +921,7 @@ attn_merge_small_kernel(const float* __restrict__ part_o, const float2* __restri
 }
 
 fr_status launch_merge(const float* part_o, const float2* part_ml, float* out, int M, int splits, int hd,
-                       int rstride, cudaStream_t stream) {
+                       int rstride, unsigned* ws, cudaStream_t stream) {
     if (splits < 1 || splits > kMaxMergeSplits) return FR_ERR_UNSUPPORTED;
     cudaLaunchConfig_t cfg;
     memset(&cfg, 0, sizeof(cfg));
@@ -945,9 +978,9 @@ fr_status launch_merge(const float* part_o, const float2* part_ml, float* out, i
     cfg.numAttrs = 1;
     cudaError_t e;
     switch (hd) {
-        case 64: e = cudaLaunchKernelEx(&cfg, attn_merge_kernel<64>, part_o, part_ml, out, M, splits, nw, early, rstride); break;
-        case 128: e = cudaLaunchKernelEx(&cfg, attn_merge_kernel<128>, part_o, part_ml, out, M, splits, nw, early, rstride); break;
-        default: e = cudaLaunchKernelEx(&cfg, attn_merge_kernel<256>, part_o, part_ml, out, M, splits, nw, early, rstride); break;
+        case 64: e = cudaLaunchKernelEx(&cfg, attn_merge_kernel<64>, part_o, part_ml, out, M, splits, nw, early, rstride, ws); break;
+        case 128: e = cudaLaunchKernelEx(&cfg, attn_merge_kernel<128>, part_o, part_ml, out, M, splits, nw, early, rstride, ws); break;
+        default: e = cudaLaunchKernelEx(&cfg, attn_merge_kernel<256>, part_o, part_ml, out, M, splits, nw, early, rstride, ws); break;
     }
     return e == cudaSuccess ? FR_OK : FR_ERR_CUDA;
 }

@@ -759,7 +759,7 @@ static fr_status decode_attn_impl(const uint16_t* q16, const float* q, int64_t q
         L.bn = p.bn;
         const fr_status st = tc::launch_tc(L, hd, stream);
         if (st != FR_OK || !p.merge_kernel) return st;
-        return tc::launch_merge(a.part_o, a.part_ml, out, M, p.splits, hd, 128, stream);
+        return tc::launch_merge(a.part_o, a.part_ml, out, M, p.splits, hd, 128, a.status, stream);
     }
 
     const Plan p = make_plan(M, n_kv, sms, o.force_splits);
