@@ -759,7 +759,7 @@ attn_tc_kernel(const __grid_constant__ TcArgs a, const __grid_constant__ Maps mp
 // + rr)*HD] (rstride = 128 for the 128-row tiles, M for the keys-on-M kernel).
 // A unit is one (row,
 // 128-column chunk); it gets nw warps (one per split when that fits the GPU in
-// one wave, else one per 6 splits, see launch_merge) and a CTA of up to
+// one wave, else one per 5 or 6 splits, see launch_merge) and a CTA of up to
 // kMergeWarps warps holds several units. Warp w of a unit takes splits
 // w, w + nw, ... (at most a handful each, so the loads of the whole CTA are in
 // flight together). Each warp weighs its splits by 2^(m_s - m_w) against its
@@ -767,7 +767,12 @@ attn_tc_kernel(const __grid_constant__ TcArgs a, const __grid_constant__ Maps mp
 // against the row maximum. The order of every sum is fixed: the result does
 // not depend on timing.
 constexpr int kMergeWarps = 32;
-constexpr int kMergeSplitsPerWarp = 6;          // nw = ceil(splits / 6) warps per unit
+// Splits per warp when a unit cannot have one warp per split: nw = ceil(splits /
+// this) warps per unit. At hd <= 128 a row is one unit, so there are half as
+// many units and 5 splits per warp (more warps each) pays: hd 128 / 16 tokens
+// / 65536 keys 18.70 -> 17.75 us per call, long decode 25.06 -> 23.82 us,
+// while at hd 256 it cost 0.2-0.4 us (same-process A/B).
+__host__ __device__ constexpr int merge_splits_per_warp(int hd) { return hd >= 256 ? 6 : 5; }
 
 // The FR_TRACE build holds the untraced kernel's register count (two CTAs of
 // up to 1024 threads per SM), so that its stamps do not change the occupancy.
@@ -783,9 +788,9 @@ attn_merge_kernel(const float* __restrict__ part_o, const float2* __restrict__ p
     constexpr int CWM = HD < 128 ? HD : 128;
     constexpr int NCH = HD / CWM;
     constexpr int LANES = CWM / 4;
-    constexpr int PER_WARP = kMergeSplitsPerWarp;
+    constexpr int PER_WARP = merge_splits_per_warp(HD);
     static_assert(PER_WARP <= 32, "one (m, l) pair per lane");
-    static_assert((kMaxMergeSplits + kMergeSplitsPerWarp - 1) / kMergeSplitsPerWarp <= kMergeWarps,
+    static_assert((kMaxMergeSplits + PER_WARP - 1) / PER_WARP <= kMergeWarps,
                   "every split count fits in one CTA");
     __shared__ float s_acc[kMergeWarps][CWM];
     __shared__ float s_m[kMergeWarps], s_l[kMergeWarps];
@@ -956,14 +961,15 @@ fr_status launch_merge(const float* part_o, const float2* part_ml, float* out, i
         return FR_ERR_CUDA;
     // Warps per unit and units per CTA. When one warp per split fits the GPU in
     // one wave, take that (the fewest dependent loads per warp). Otherwise up to
-    // 6 splits per warp (fewer instructions per split), with few enough units
-    // per CTA that the grid still covers the SMs.
+    // 5 (hd <= 128) or 6 splits per warp (fewer instructions per split), with
+    // few enough units per CTA that the grid still covers the SMs.
     int nw, upc;
     if ((int64_t)units * splits <= (int64_t)sms * kMergeWarps && splits <= kMergeWarps) {
         nw = splits;
         upc = kMergeWarps / nw;
     } else {
-        nw = (splits + kMergeSplitsPerWarp - 1) / kMergeSplitsPerWarp;
+        const int spw = merge_splits_per_warp(hd);
+        nw = (splits + spw - 1) / spw;
         upc = kMergeWarps / nw;
         if (upc > units / sms) upc = units / sms > 0 ? units / sms : 1;
     }
