@@ -222,3 +222,16 @@ def test_noalloc_size_limit_matches_the_documented_thresholds(lib):
     assert fits(1520, 8, 128) and not fits(1521, 8, 128)        # M 12160 | 12168
     assert fits(3008, 8, 64) and not fits(3009, 8, 64)          # M 24064 | 24072
     assert fits(1, 8, 256, 65536) and fits(4, 8, 128, 65536)    # keys-on-M plans need only the Q slot
+
+
+def test_trace_build_compiles_and_exports_the_same_abi():
+    """The timeline-instrumented variant (FR_TRACE, used by
+    `python -m gqa_kv_head_gb300.trace`) builds into its own directory,
+    loads without a GPU and exports every declared function; the library
+    itself stays uninstrumented."""
+    from gqa_kv_head_gb300 import build
+    path = build.build(trace=True)
+    assert os.path.realpath(path) != os.path.realpath(build.library_path())
+    tr = ctypes.CDLL(path)
+    for n in sorted(_declared()):
+        assert hasattr(tr, n), f"{n} missing from the FR_TRACE build"
