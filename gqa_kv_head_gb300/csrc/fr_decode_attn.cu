@@ -420,24 +420,26 @@ static bool sw_shape_ok(int n_tok, int n_head, int hd) {
 // The library's choice of the keys-on-M kernel and its slice size (measured
 // on GB300, graph replay of fused calls, against the 128-row kernel):
 //  (a) 16-row slices when the KV range is short: n_kv >= 1024 and
-//      ceil(M/16) * n_kv <= 16384 (each CTA then streams at most ~16384
-//      keys' worth of its split): 8-19 % faster at 1024-2048 keys for every
-//      M up to 128, even at the limit (4096 keys for 64 rows, 8192 for 32);
-//      beyond it the slices' repeated reads of each K/V tile cost more than
-//      they save, and below 1024 keys the 128-row kernel's short call wins;
+//      ceil(M/16) * n_kv <= 32768 at hd 256, <= 16384 at hd 128 (the slices'
+//      repeated reads of each K/V tile, served by L2, stay cheaper than the
+//      128-row kernel's split states): at hd 256 4-20 % faster up to the
+//      limit (128 rows / 4096 keys 12.42 vs 12.95 us, 64 / 8192 12.57 vs
+//      13.63, 32 / 16384 12.86 vs 13.69), slower past it (128 / 8192 16.01 vs
+//      14.58); at hd 128 the limit is 16384 (128 / 4096: 10.62 vs 10.23);
+//      below 1024 keys the 128-row kernel's short call wins;
 //  (b) one slice of all rows for M <= 32 and n_kv >= max(1024, 256 M):
 //      10-25 % faster on long KV;
-//  (c) 32-row slices for hd 128, 32 < M <= 64 and n_kv >= 16384: 3-7 %
-//      faster (two CTAs per split read each tile);
-// else the 128-row kernel. Returns the rows per slice, or 0 for layout 1.
+// else the 128-row kernel (32-row slices for 33-64 rows at hd 128 were 3-7 %
+// faster once, and tie or lose since the merge kernel takes 5 splits per
+// warp there: 64 rows / 65536 keys 17.76 vs 17.28 us). Returns the rows per
+// slice, or 0 for layout 1.
 static constexpr int kSwShortKeys = 1024;
-static constexpr int64_t kSwShortWork = 16384;
+static int64_t sw_short_work(int hd) { return hd == 256 ? 32768 : 16384; }
 static int auto_sw_rows(int n_tok, int n_head, int hd, int n_kv) {
     if (!sw_shape_ok(n_tok, n_head, hd)) return 0;
     const int M = n_tok * n_head;
-    if (n_kv >= kSwShortKeys && (int64_t)((M + 15) / 16) * n_kv <= kSwShortWork) return 16;
+    if (n_kv >= kSwShortKeys && (int64_t)((M + 15) / 16) * n_kv <= sw_short_work(hd)) return 16;
     if (M <= 32 && n_kv >= kSwShortKeys && n_kv >= 256 * M) return sw::rows_n(M);
-    if (hd == 128 && M > 32 && M <= 64 && n_kv >= 16384) return 32;
     return 0;
 }
 // Kernel of a call: 1 = 128-row query tiles (fr_attn_tc.cu, or the mma.sync

@@ -253,9 +253,9 @@ typedef struct fr_attn_opts {
                               query rows as its N (M <= 128 rows, hd 128 or 256, n_tok <= 16:
                               FR_ERR_UNSUPPORTED otherwise). The library's choice (measured
                               faster there) is 2 with 16-row slices when n_kv >= 1024 and
-                              ceil(M/16) * n_kv <= 16384; 2 with one slice of all rows when
-                              M <= 32 and n_kv >= max(1024, 256 M); 2 with 32-row slices when
-                              hd = 128, 32 < M <= 64 and n_kv >= 16384; else 1 — unless
+                              ceil(M/16) * n_kv <= 32768 (hd 256) or 16384 (hd 128); 2 with
+                              one slice of all rows when M <= 32 and n_kv >= max(1024, 256 M);
+                              else 1 — unless
                               force_cluster or merge_mode 1 is given (then 1). */
     int slice_rows;        /* layout 2 only: 0 = library's choice; else 16, 32 or 64 query
                               rows per CTA (the MMA's N): the M rows are cut into

@@ -34,18 +34,15 @@ KOM = dict(layout=2)
 def _auto_rows(w):
     """Rows per slice of the library's own keys-on-M choice (0: the 128-row
     kernel), as include/fr_kernels.h documents it: 16-row slices for a short
-    KV range (n_kv >= 1024 and ceil(M/16)*n_kv <= 16384), one slice of all
-    rows for M <= 32 and n_kv >= max(1024, 256 M), 32-row slices for hd 128,
-    32 < M <= 64 and n_kv >= 16384."""
+    KV range (n_kv >= 1024 and ceil(M/16)*n_kv <= 32768 at hd 256, 16384 at
+    hd 128), one slice of all rows for M <= 32 and n_kv >= max(1024, 256 M)."""
     M = w.n_tok * w.n_head
     if w.hd not in (128, 256) or w.n_tok > 16 or M > 128:
         return 0
-    if w.n_kv >= 1024 and -(-M // 16) * w.n_kv <= 16384:
+    if w.n_kv >= 1024 and -(-M // 16) * w.n_kv <= (32768 if w.hd == 256 else 16384):
         return 16
     if M <= 32 and w.n_kv >= max(1024, 256 * M):
         return 16 if M <= 16 else 32
-    if w.hd == 128 and 32 < M <= 64 and w.n_kv >= 16384:
-        return 32
     return 0
 
 
